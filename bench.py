@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV cache decode hot path on GB300.
+
+One step = one pass of the whole path over one batch: the batched
+copy-on-write block copy (when the workload has copies), the KV write of every
+sequence's new token, and decode attention (partitioned pass + merge) -- all
+through the library's C ABI.  Inputs are resident in HBM when timing starts;
+L2 is flushed (256 MiB write) before every timed step, outside the timed span.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workload llama8b]
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_117_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+UNIT = "GB/s"
+FLUSH_BYTES = 256 << 20
+TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="llama8b", choices=sorted(TABLE_WIDTH_TOKENS))
+    ap.add_argument("--partition", type=int, default=None,
+                    help="partition_tokens (default: the workload's, 512)")
+    ap.add_argument("--cpu-seqs", type=int, default=256,
+                    help="sequences in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload and its algorithmic bytes
+
+def build_metadata(w):
+    lens = wl.context_lens(w)
+    tables = wl.scatter_block_tables(lens, w.block_size, wl.free_block_order(w))
+    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    return lens, tables, width
+
+
+def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0):
+    """Bytes the step must move at minimum: every valid K/V row of every
+    (sequence, KV head) once, q, the used block-table entries, lengths, the
+    output, the split-context records (written and read back once), the new
+    K/V rows in and out, and the copied blocks."""
+    es = w.elem_bytes
+    S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    part_blocks = width if pt == 0 else pt // B
+    nb = [-(-L // B) for L in lens]
+    nparts = [-(-n // part_blocks) if n else 0 for n in nb]
+    multi = [p for p in nparts if p > 1]
+    kv = sum(lens) * Hkv * D * es * 2
+    rec = sum(multi) * Hq * (D + 2) * 4
+    decode = (kv + S * Hq * D * es + sum(nb) * 4 + S * 4
+              + (S - len(multi)) * Hq * D * out_es + rec)
+    merge = rec + len(multi) * Hq * D * out_es + (S * 4 if multi or part_blocks < width else 0)
+    write = S * Hkv * D * es * 2 * 2 + S * 8
+    block_bytes = B * Hkv * D * es
+    copy = n_pairs * block_bytes * 2 * 2 + n_pairs * 16
+    return {"kv": kv, "decode": decode, "merge": merge, "write": write, "copy": copy,
+            "attention": decode + merge, "step": decode + merge + write + copy}
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_desc(w, width):
+    lk = {"lognormal": "lognormal lengths (median %g, sigma %g, clipped to [%d, %d])",
+          "uniform": "uniform lengths in [%d, %d]", "fixed": "fixed lengths"}[w.lens_kind]
+    lk = lk % w.lens_args if w.lens_kind != "fixed" else \
+        f"fixed lengths {sorted(set(w.lens_args))}"
+    return (f"{w.name}: {w.num_seqs} seqs, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
+            f"head_dim {w.head_dim}, {str(w.dtype).replace('torch.', '')}, block {w.block_size}, "
+            f"{lk}, {w.num_blocks}-block pool, blocks scattered by a seeded permutation, "
+            f"table width {width}, q/K/V ~ N(0,1), one new token per seq")
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the only place bench.py touches oracle/)
+
+def sample_blocks(tables, nseq):
+    seqs = list(range(min(nseq, len(tables))))
+    return seqs, sorted({b for s in seqs for b in tables[s]})
+
+
+def oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value, slots, seqs):
+    """fp64 oracle over ``seqs``: KV write then attention, on a compact CPU
+    pool ``kc``/``vc`` holding the blocks ``ids``.  Returns (seconds,
+    algorithmic bytes of the sample, threads used)."""
+    import oracle.paged_ops as ops
+    remap = {b: i for i, b in enumerate(ids)}
+    B = w.block_size
+    loc_slots = [remap[slots[s] // B] * B + slots[s] % B for s in seqs]
+    tabs = [[remap[b] for b in tables[s]] for s in seqs]
+    qc, kk, vv = q[seqs].cpu(), key[seqs].cpu(), value[seqs].cpu()
+    kc, vc = kc.clone(), vc.clone()
+    t0 = time.perf_counter()
+    ops.write_kv(kc, vc, kk, vv, loc_slots)
+    ops.attend(qc, kc, vc, tabs, [lens[s] for s in seqs], w.scale)
+    dt = time.perf_counter() - t0
+    nbytes = algorithmic_bytes(w, [lens[s] for s in seqs], width, 0, w.elem_bytes)
+    return dt, nbytes["kv"] + nbytes["write"], torch.get_num_threads()
+
+
+# ---------------------------------------------------------------------------
+
+def run_native(a, world, rank, local):
+    import paged_kv_cache_117_gb300 as pkv
+    from paged_kv_cache_117_gb300 import build as pbuild
+    if rank == 0:
+        pbuild.build()
+    barrier(world)
+    pkv.load()
+    assert torch.cuda.is_available(), "the native benchmark needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[a.workload]
+    pt = w.partition_tokens if a.partition is None else a.partition
+    lens, tables, width = build_metadata(w)
+    tab_cpu = wl.pad_tables(tables, width)
+    lens_cpu = torch.tensor(lens, dtype=torch.int32)
+    slots_cpu = pkv.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size)
+    k, v = wl.make_pool_chunked(w, dev)
+    q, key, value = wl.make_step_inputs(w, dev)
+    tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
+    pairs = torch.zeros((0, 2), dtype=torch.int64, device=dev)
+    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
+    nws = pkv.paged_attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
+                                              width * w.block_size, pt)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0])
+    max_parts = -(-width // (width if pt == 0 else pt // w.block_size))
+    launches_per_step = (1 if pairs.shape[0] else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+
+    # CPU-oracle sample: inputs snapshot before any library kernel runs
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        seqs, ids = sample_blocks(tables, a.cpu_seqs)
+        idx = torch.tensor(ids, device=dev)
+        dt, b, threads = oracle_sample_time(w, lens, tables, width, k[idx].cpu(), v[idx].cpu(),
+                                            ids, q, key, value, slots_cpu.tolist(), seqs)
+        cpu = {"value": b / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle (torch CPU ops) KV write + attention of the first "
+                         f"{min(a.cpu_seqs, w.num_seqs)} of {w.num_seqs} sequences, "
+                         f"{dt:.1f} s; bytes = unique K/V rows read + new rows written"}
+
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(d0=None, d1=None):
+        if pairs.shape[0]:
+            pkv.paged_block_copy(k, v, pairs)
+        pkv.paged_kv_write(key, value, k, v, slots)
+        if d0 is not None:
+            d0.record(stream)
+        pkv.paged_attention_decode(out, q, k, v, tab, lens_t, w.scale, partition_tokens=pt,
+                                   workspace=ws)
+        if d1 is not None:
+            d1.record(stream)
+
+    for _ in range(max(3, a.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) == 0
+
+    K = a.steps
+    evs = [(ev(), ev(), ev(), ev()) for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s0, s1, d0, d1 in evs:
+        flush.zero_()
+        s0.record(stream)
+        step(d0, d1)
+        s1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    step_ms = sum(s0.elapsed_time(s1) for s0, s1, _, _ in evs) / K
+    dec_ms = sum(d0.elapsed_time(d1) for _, _, d0, d1 in evs) / K
+    step_ms = max_over_ranks(world, step_ms, dev)
+    dec_ms = max_over_ranks(world, dec_ms, dev)
+
+    # end to end: per-step inputs from pinned host memory, result back to host
+    h_q, h_key, h_val = (t.cpu().pin_memory() for t in (q, key, value))
+    h_tab, h_lens, h_slots = (t.pin_memory() for t in (tab_cpu, lens_cpu, slots_cpu))
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_key, h_val, h_tab, h_lens, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_evs = [(ev(), ev()) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for e0, e1 in e2e_evs:
+        flush.zero_()
+        e0.record(stream)
+        q.copy_(h_q, non_blocking=True)
+        key.copy_(h_key, non_blocking=True)
+        value.copy_(h_val, non_blocking=True)
+        tab.copy_(h_tab, non_blocking=True)
+        lens_t.copy_(h_lens, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / K, dev)
+    assert pkv.read_device_flags(clear=True) == 0
+
+    peak, peak_kind = peak_hbm()
+    achieved = nbytes["attention"] / (dec_ms * 1e-3) / 1e9
+    value_gbs = world * nbytes["step"] / (step_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value_gbs, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": str(w.dtype).replace("torch.", "").replace("bfloat16", "bf16").replace("float16", "f16"),
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w, width), "partition_tokens": pt,
+                   "out_dtype": str(out.dtype).replace("torch.", ""),
+                   "l2": "flushed before every step (256 MiB write, outside the timed span)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "pct_of_peak": round(100 * value_gbs / world / peak, 1),
+        "seq_steps_per_s": round(world * w.num_seqs / (step_ms * 1e-3), 1),
+        "attention_ms": round(dec_ms, 4),
+        "bytes_per_step": nbytes,
+        "roofline": {"kernel": "paged_attention_decode (partitioned pass + merge)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": round(world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 4),
+        "cpu_baseline": cpu,
+    }
+    return res
+
+
+def run_reference(a, world, rank, local):
+    """The fp64 CPU oracle as it stands, one bounded sample per step."""
+    if rank != 0:
+        return None
+    w = wl.WORKLOADS[a.workload]
+    lens, tables, width = build_metadata(w)
+    # inputs with the same distributions, generated on the CPU for just the
+    # blocks the sample reads (no GPU needed)
+    nseq = max(1, min(w.num_seqs, 4))
+    seqs, ids = sample_blocks(tables, nseq)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    shape = (len(ids), w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.randn(shape, generator=g).to(w.dtype)
+    vc = torch.randn(shape, generator=g).to(w.dtype)
+    q, key, value = wl.make_step_inputs(w, "cpu")
+    tab_cpu = wl.pad_tables(tables, width)
+    lens_cpu = torch.tensor(lens, dtype=torch.int32)
+    import paged_kv_cache_117_gb300.binding as bnd
+    slots = bnd.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size).tolist()
+    times, nbytes, threads = [], 0, torch.get_num_threads()
+    for i in range(max(3, a.warmup) + a.steps):
+        dt, b, threads = oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value,
+                                            slots, seqs)
+        if i >= max(3, a.warmup):
+            times.append(dt)
+            nbytes = b
+    ms = 1e3 * sum(times) / len(times)
+    val = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"fp64 oracle KV write + attention of the first {nseq} of {w.num_seqs} sequences "
+              f"per step ({nbytes / 1e6:.1f} MB algorithmic)")
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": UNIT,
+            "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w, width)},
+            "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    a = parse_args()
+    world, rank, local = dist_init()
+    if a.impl == "reference":
+        res = run_reference(a, world, rank, local)
+    else:
+        res = run_native(a, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 (sm_103a) paged KV cache decode library.
+ *
+ * The library implements the data-parallel hot path of PagedAttention: the
+ * KV cache lives in one pool of fixed-size blocks, and every sequence reaches
+ * its tokens through its own block table.  Three operations keep that pool
+ * live and read it:
+ *
+ *   paged_kv_write          store this step's new keys/values into the slots
+ *                           the block manager assigned ("reshape and cache")
+ *   paged_block_copy        the batched copy-on-write block copy
+ *   paged_attention_decode  single-query attention over the paged context
+ *
+ * Sources for what each call computes: "PagedAttention and vLLM: Paging the
+ * KV Cache Like an OS" (vidyal.ai), Step 5, the three kernels (write, read and
+ * attend, copy) and Step 4 (reference counts and copy-on-write);
+ * "PagedAttention" (tensortonic.com), section 5 (write before attending,
+ * softmax over all valid positions, the table [3, 0, 6]);
+ * "PagedAttention: Virtual Memory for the KV Cache" (alexdo.xyz), the
+ * block-wise attention equation.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, dense
+ *    (row-major, no padding) and 16-byte aligned.  The library allocates no
+ *    memory: scratch for the split-context pass is passed in (see
+ *    paged_attention_workspace_bytes).
+ *  - Pool layout: k_cache and v_cache are [num_blocks, block_size,
+ *    num_kv_heads, head_dim] of the cache dtype.  Slot s of the pool is
+ *    (block s / block_size, offset s % block_size).
+ *  - Supported shapes: head_dim in {64, 128}; block_size in {4, 8, 16, 32};
+ *    cache dtype PKV_F16 or PKV_BF16; num_q_heads a multiple of num_kv_heads.
+ *  - Query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are found on the host before anything
+ *    is launched and returned as a status; nothing is launched then.  A
+ *    launch failure returns PKV_ERR_CUDA.  Calls never abort the process.
+ *  - Device-side values (block ids, slots, lengths, copy pairs) are checked
+ *    inside the kernels: an out-of-range value is never dereferenced; the
+ *    access is skipped (or the length clamped), and a bit is set in the
+ *    library's device flag word, read back with pkv_read_device_flags.
+ *  - Results of calls that overlap in time on the same buffers are undefined;
+ *    order them on one stream: block copy, then write, then attend.
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pkv_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,      /* a required pointer is NULL */
+  PKV_ERR_SHAPE = 2,     /* unsupported or inconsistent sizes */
+  PKV_ERR_DTYPE = 3,     /* unsupported dtype */
+  PKV_ERR_RANGE = 4,     /* a size is negative or too large */
+  PKV_ERR_ALIAS = 5,     /* buffers that must be distinct overlap */
+  PKV_ERR_CUDA = 6,      /* a CUDA runtime / driver call failed */
+  PKV_ERR_WORKSPACE = 7, /* workspace missing or too small */
+  PKV_ERR_ALIGN = 8      /* a pointer is not 16-byte aligned */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+/* Bits of the device flag word. */
+#define PKV_FLAG_BLOCK_RANGE 0x1u /* a block table entry was outside [0, num_blocks) */
+#define PKV_FLAG_SLOT_RANGE 0x2u  /* a slot was >= num_blocks * block_size */
+#define PKV_FLAG_PAIR_RANGE 0x4u  /* a copy pair named a block outside the pool */
+#define PKV_FLAG_LEN_RANGE 0x8u   /* a context length was < 0 or > max_blocks * block_size */
+#define PKV_FLAG_TIMEOUT 0x10u    /* a kernel gave up waiting on its own tile loads */
+
+/*
+ * paged_kv_write -- store new keys/values into their slots.
+ *
+ * "The key and value are written to its assigned block and offset"
+ * ("PagedAttention", section 5); the write kernel is one fused launch for all
+ * tokens ("PagedAttention and vLLM ...", Step 5, "Write").
+ *
+ *   key, value    [num_tokens, num_kv_heads, head_dim], cache dtype
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping  int64 [num_tokens]; token t goes to slot slot_mapping[t]
+ *                 (= block * block_size + offset).  A negative slot skips the
+ *                 token.  A slot >= num_blocks * block_size is skipped and
+ *                 flagged (PKV_FLAG_SLOT_RANGE).
+ *
+ * The copy is bit-exact.  Two tokens naming one slot race (one of them wins).
+ * num_tokens == 0 is a no-op that launches nothing.
+ */
+pkv_status paged_kv_write(const void *key, const void *value, void *k_cache,
+                          void *v_cache, const int64_t *slot_mapping,
+                          int num_tokens, int num_blocks, int block_size,
+                          int num_kv_heads, int head_dim, pkv_dtype dtype,
+                          pkv_stream_t stream);
+
+/*
+ * paged_block_copy -- batched copy-on-write block copy.
+ *
+ * "Copy-on-write can trigger many small block copies in one step, so one
+ * kernel batches them" ("PagedAttention and vLLM ...", Step 5, "Copy").  For
+ * every pair, all block_size slots of block src are copied to block dst, in
+ * k_cache and in v_cache, bit-exactly, in one launch.
+ *
+ *   block_pairs  int64 [num_pairs][2] = (src, dst), DEVICE memory.
+ *
+ * Preconditions (the block manager's invariants; not checked on the host
+ * because the pairs live on the device): every dst appears once and no dst is
+ * also a src in the same call.  A pair naming a block outside [0, num_blocks)
+ * is skipped and flagged (PKV_FLAG_PAIR_RANGE).  num_pairs == 0 is a no-op.
+ */
+pkv_status paged_block_copy(void *k_cache, void *v_cache,
+                            const int64_t *block_pairs, int num_pairs,
+                            int num_blocks, int block_size, int num_kv_heads,
+                            int head_dim, pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * paged_attention_decode -- single-query attention over the paged context.
+ *
+ * For sequence s and query head hq (KV head h = hq / G):
+ *   out[s, hq, :] = sum_t softmax_t(scale * q[s, hq, :] . K_t) V_t
+ * over the L_s = context_lens[s] tokens of the sequence, token t read from
+ * physical block block_tables[s, t / block_size], offset t % block_size
+ * ("PagedAttention and vLLM ...", Step 5; "PagedAttention", sections 4-5).
+ * The softmax is over all L_s positions at once; slots of the last block at
+ * or past L_s are never read.  L_s counts this step's token, which must
+ * already be written (paged_kv_write earlier on the same stream).  L_s == 0
+ * gives zeros.
+ *
+ *   out            [num_seqs, num_q_heads, head_dim] of out_dtype (F32, F16
+ *                  or BF16; arithmetic is fp32 regardless)
+ *   q              [num_seqs, num_q_heads, head_dim], cache dtype
+ *   block_tables   int32 [num_seqs, max_blocks]; entries past a sequence's
+ *                  last block are ignored
+ *   context_lens   int32 [num_seqs]; a length outside [0, max_blocks *
+ *                  block_size] is clamped and flagged (PKV_FLAG_LEN_RANGE)
+ *   scale          softmax scale, normally 1/sqrt(head_dim)
+ *   partition_tokens
+ *                  0: one pass per sequence.  Otherwise a multiple of
+ *                  block_size: each sequence's context is cut into partitions
+ *                  of this many tokens, processed in parallel, and merged by a
+ *                  second launch that rescales by each partition's running
+ *                  max (log-sum-exp merge).
+ *   workspace      device scratch of at least
+ *                  paged_attention_workspace_bytes(num_seqs, num_q_heads,
+ *                  head_dim, max_blocks * block_size, partition_tokens)
+ *                  bytes; may be NULL when that is 0.  Contents on entry do
+ *                  not matter.
+ */
+pkv_status paged_attention_decode(
+    void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
+    const void *v_cache, pkv_dtype dtype, const int32_t *block_tables,
+    int max_blocks, const int32_t *context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, float scale, int partition_tokens, void *workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Scratch bytes paged_attention_decode needs: one (max, sum, head_dim-wide
+ * unnormalised output) record in fp32 per (sequence, query head, partition),
+ * for ceil(max_context / partition_tokens) partitions.  max_context is the
+ * capacity of one block-table row (max_blocks * block_size).  Returns 0 when
+ * partition_tokens is 0 or at most one partition fits; returns (size_t)-1 on
+ * invalid arguments.
+ */
+size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
+                                       int head_dim, int max_context,
+                                       int partition_tokens);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *pkv_status_string(pkv_status status);
+
+/*
+ * Read (and with clear != 0, reset) the library's device flag word for the
+ * current device.  Synchronises `stream` first so every earlier call on it
+ * has finished.  *flags_out receives an OR of PKV_FLAG_* bits.
+ */
+pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear,
+                                 pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H */

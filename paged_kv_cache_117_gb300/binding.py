@@ -1,0 +1,181 @@
+"""Thin ctypes binding over the C ABI in ``include/paged_kv.h``.
+
+Argument marshalling only: every step of the path runs in the CUDA library.
+There is no fallback: if ``libpaged_kv.so`` is missing or fails to load, every
+call raises.  Functions take CUDA tensors laid out as the header describes and
+launch on the current torch stream (or the ``stream`` given).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libpaged_kv.so")
+
+PKV_F16, PKV_BF16, PKV_F32 = 0, 1, 2
+_DTYPE_CODE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
+
+FLAG_BLOCK_RANGE = 0x1
+FLAG_SLOT_RANGE = 0x2
+FLAG_PAIR_RANGE = 0x4
+FLAG_LEN_RANGE = 0x8
+FLAG_TIMEOUT = 0x10
+
+EXPORTED_SYMBOLS = (
+    "paged_kv_write",
+    "paged_block_copy",
+    "paged_attention_decode",
+    "paged_attention_workspace_bytes",
+    "pkv_status_string",
+    "pkv_read_device_flags",
+)
+
+
+class PkvError(RuntimeError):
+    def __init__(self, func: str, status: int, text: str):
+        super().__init__(f"{func}: status {status} ({text})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it is missing: there is no
+    fallback path."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library not found at {p}; build it with "
+            "`python -m paged_kv_cache_117_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(p)
+    vp, ci, cf, cs = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.paged_kv_write.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp]
+    lib.paged_kv_write.restype = ci
+    lib.paged_block_copy.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp]
+    lib.paged_block_copy.restype = ci
+    lib.paged_attention_decode.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, ci, ci, ci,
+                                           ci, ci, ci, cf, ci, vp, cs, vp]
+    lib.paged_attention_decode.restype = ci
+    lib.paged_attention_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+    lib.paged_attention_workspace_bytes.restype = cs
+    lib.pkv_status_string.argtypes = [ci]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci, vp]
+    lib.pkv_read_device_flags.restype = ci
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(func: str, status: int) -> None:
+    if status != 0:
+        raise PkvError(func, status, load().pkv_status_string(status).decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(name: str, *ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError(f"{name}: tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: tensors must be contiguous")
+
+
+def _cache_dims(k_cache: torch.Tensor):
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [num_blocks, block_size, num_kv_heads, head_dim]")
+    return tuple(int(x) for x in k_cache.shape)
+
+
+def paged_kv_write(key, value, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """Store key/value [T, Hkv, D] into the pool slots slot_mapping (int64 [T])."""
+    _need_cuda("paged_kv_write", key, value, k_cache, v_cache, slot_mapping)
+    N, B, H, D = _cache_dims(k_cache)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    st = load().paged_kv_write(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(slot_mapping), int(key.shape[0]), N, B, H, D,
+                               _DTYPE_CODE.get(k_cache.dtype, -1), _stream(stream))
+    _check("paged_kv_write", st)
+
+
+def paged_block_copy(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst for every row (src, dst) of int64 [P, 2]."""
+    _need_cuda("paged_block_copy", k_cache, v_cache, block_pairs)
+    N, B, H, D = _cache_dims(k_cache)
+    if block_pairs.dtype != torch.int64:
+        raise ValueError("block_pairs must be int64")
+    P = int(block_pairs.shape[0]) if block_pairs.numel() else 0
+    st = load().paged_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, N, B,
+                                 H, D, _DTYPE_CODE.get(k_cache.dtype, -1), _stream(stream))
+    _check("paged_block_copy", st)
+
+
+def paged_attention_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                                    max_context: int, partition_tokens: int) -> int:
+    n = load().paged_attention_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                               max_context, partition_tokens)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid workspace query")
+    return int(n)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           partition_tokens=512, workspace=None, stream=None):
+    """Decode attention: out [S, Hq, D] (f32, f16 or bf16) from q [S, Hq, D]
+    over the paged pool.  A workspace tensor is allocated by torch when none is
+    given and the partitioned pass needs one."""
+    _need_cuda("paged_attention_decode", out, q, k_cache, v_cache, block_tables, context_lens)
+    N, B, Hkv, D = _cache_dims(k_cache)
+    S, Hq, _ = (int(x) for x in q.shape)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    max_blocks = int(block_tables.shape[1])
+    need = paged_attention_workspace_bytes(S, Hq, D, max_blocks * B, partition_tokens)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().paged_attention_decode(
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables), max_blocks, _ptr(context_lens),
+        S, Hq, Hkv, D, B, N, float(scale), int(partition_tokens), _ptr(workspace), ws_bytes,
+        _stream(stream))
+    _check("paged_attention_decode", st)
+    return out
+
+
+def read_device_flags(clear: bool = True, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    st = load().pkv_read_device_flags(ctypes.byref(v), 1 if clear else 0, _stream(stream))
+    _check("pkv_read_device_flags", st)
+    return int(v.value)
+
+
+def decode_slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor,
+                        block_size: int) -> torch.Tensor:
+    """Slot of each sequence's newest token (position L_s - 1):
+    table[s][(L_s - 1) // B] * B + (L_s - 1) % B; -1 for empty sequences.
+    Host-side helper for building a decode step's slot_mapping."""
+    lens = context_lens.to(torch.int64).cpu()
+    tabs = block_tables.to(torch.int64).cpu()
+    pos = (lens - 1).clamp(min=0)
+    blk = tabs.gather(1, (pos // block_size).unsqueeze(1)).squeeze(1)
+    slots = blk * block_size + pos % block_size
+    return torch.where(lens > 0, slots, torch.full_like(slots, -1))

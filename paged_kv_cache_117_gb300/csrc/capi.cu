@@ -1,0 +1,301 @@
+// The library's C ABI (declared in include/paged_kv.h): host-side argument
+// checks, TMA descriptor encoding for the pool, and the kernel launches.
+#include <limits.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_launch.h"
+
+// OR of PKV_FLAG_* bits raised by the kernels on this device.
+__device__ unsigned int g_pkv_flags;
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+constexpr int MAX_DEVICES = 64;
+
+unsigned *device_flags() {
+  static unsigned *ptrs[MAX_DEVICES] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_flags) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned *>(p);
+  }
+  return ptrs[dev];
+}
+
+// TMA descriptor over one pool [N, B, Hkv, D] whose box is one KV head's
+// [B, D] tile of one block.  A few recent descriptors are cached per thread.
+struct MapKey {
+  const void *base;
+  int dt, n, b, h, d;
+  bool operator==(const MapKey &o) const {
+    return base == o.base && dt == o.dt && n == o.n && b == o.b && h == o.h && d == o.d;
+  }
+};
+
+bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, int Hkv, int D) {
+  struct Entry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+  };
+  thread_local Entry cache[4] = {};
+  thread_local int next = 0;
+  const MapKey key{base, (int)dt, N, B, Hkv, D};
+  for (auto &e : cache)
+    if (e.used && e.key == key) {
+      *out = e.map;
+      return true;
+    }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t es = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)B, (cuuint64_t)N};
+  cuuint64_t strides[3] = {D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)B * Hkv * D * es};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)B, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  const CUtensorMapDataType t =
+      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(&map, t, 4, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  cache[next] = Entry{key, map, true};
+  next = (next + 1) & 3;
+  *out = map;
+  return true;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool supported_cache_dtype(pkv_dtype d) { return d == PKV_F16 || d == PKV_BF16; }
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+bool supported_block(int b) { return b == 4 || b == 8 || b == 16 || b == 32; }
+
+size_t dtype_bytes(pkv_dtype d) { return d == PKV_F32 ? 4 : 2; }
+
+long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "null pointer";
+    case PKV_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case PKV_ERR_DTYPE: return "unsupported dtype";
+    case PKV_ERR_RANGE: return "size out of range";
+    case PKV_ERR_ALIAS: return "buffers overlap";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_ALIGN: return "pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                       int max_context, int partition_tokens) {
+  if (num_seqs < 0 || num_q_heads < 0 || head_dim <= 0 || max_context < 0 ||
+      partition_tokens < 0)
+    return (size_t)-1;
+  if (partition_tokens == 0) return 0;
+  const long long parts = ceil_div_ll(max_context, partition_tokens);
+  if (parts <= 1) return 0;
+  return (size_t)num_seqs * (size_t)num_q_heads * (size_t)parts * (size_t)(head_dim + 2) *
+         sizeof(float);
+}
+
+pkv_status paged_kv_write(const void *key, const void *value, void *k_cache, void *v_cache,
+                          const int64_t *slot_mapping, int num_tokens, int num_blocks,
+                          int block_size, int num_kv_heads, int head_dim, pkv_dtype dtype,
+                          pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_RANGE;
+  if (!supported_cache_dtype(dtype)) return PKV_ERR_DTYPE;
+  if (!supported_head_dim(head_dim) || !supported_block(block_size)) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_NULL;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+    return PKV_ERR_ALIGN;
+  const size_t row = (size_t)num_kv_heads * head_dim * 2;
+  const size_t pool = (size_t)num_blocks * block_size * row;
+  const size_t in = (size_t)num_tokens * row;
+  if (overlap(k_cache, pool, v_cache, pool) || overlap(key, in, k_cache, pool) ||
+      overlap(key, in, v_cache, pool) || overlap(value, in, k_cache, pool) ||
+      overlap(value, in, v_cache, pool))
+    return PKV_ERR_ALIAS;
+  if (row > (size_t)INT_MAX) return PKV_ERR_RANGE;
+  unsigned *flags = device_flags();
+  if (!flags) return PKV_ERR_CUDA;
+  const cudaError_t e = pkv::launch_kv_write(key, value, k_cache, v_cache, slot_mapping,
+                                             num_tokens, (int)row,
+                                             (long long)num_blocks * block_size, flags,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_pairs,
+                            int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                            int head_dim, pkv_dtype dtype, pkv_stream_t stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_RANGE;
+  if (!supported_cache_dtype(dtype)) return PKV_ERR_DTYPE;
+  if (!supported_head_dim(head_dim) || !supported_block(block_size)) return PKV_ERR_SHAPE;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_NULL;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 8))
+    return PKV_ERR_ALIGN;
+  const size_t block_bytes = (size_t)block_size * num_kv_heads * head_dim * 2;
+  const size_t pool = block_bytes * num_blocks;
+  if (overlap(k_cache, pool, v_cache, pool) ||
+      overlap(block_pairs, (size_t)num_pairs * 16, k_cache, pool) ||
+      overlap(block_pairs, (size_t)num_pairs * 16, v_cache, pool))
+    return PKV_ERR_ALIAS;
+  unsigned *flags = device_flags();
+  if (!flags) return PKV_ERR_CUDA;
+  const cudaError_t e =
+      pkv::launch_block_copy(k_cache, v_cache, block_pairs, num_pairs, (long long)block_bytes,
+                             num_blocks, flags, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
+                                  const void *k_cache, const void *v_cache, pkv_dtype dtype,
+                                  const int32_t *block_tables, int max_blocks,
+                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int num_blocks, float scale, int partition_tokens,
+                                  void *workspace, size_t workspace_bytes,
+                                  pkv_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks <= 0 || partition_tokens < 0)
+    return PKV_ERR_RANGE;
+  if (!supported_cache_dtype(dtype)) return PKV_ERR_DTYPE;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16)
+    return PKV_ERR_DTYPE;
+  if (!supported_head_dim(head_dim) || !supported_block(block_size)) return PKV_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (partition_tokens % block_size != 0) return PKV_ERR_SHAPE;
+  if ((long long)max_blocks * block_size > INT_MAX) return PKV_ERR_RANGE;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return PKV_ERR_RANGE;
+  const int group = num_q_heads / num_kv_heads;
+  const int gchunks = group <= 8 ? 1 : (group + 7) / 8;
+  if ((long long)num_kv_heads * gchunks > 65535) return PKV_ERR_RANGE;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(out, dtype_bytes(out_dtype)) || !aligned(block_tables, 4) ||
+      !aligned(context_lens, 4))
+    return PKV_ERR_ALIGN;
+
+  const int part_blocks = partition_tokens == 0 ? max_blocks : partition_tokens / block_size;
+  const int max_parts = (int)ceil_div_ll(max_blocks, part_blocks);
+  const size_t need = paged_attention_workspace_bytes(
+      num_seqs, num_q_heads, head_dim, max_blocks * block_size, partition_tokens);
+  if (need == (size_t)-1) return PKV_ERR_RANGE;
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return PKV_ERR_ALIGN;
+  }
+
+  const size_t pool = (size_t)num_blocks * block_size * num_kv_heads * head_dim * 2;
+  const size_t out_sz = (size_t)num_seqs * num_q_heads * head_dim * dtype_bytes(out_dtype);
+  const size_t q_sz = (size_t)num_seqs * num_q_heads * head_dim * 2;
+  const size_t tab_sz = (size_t)num_seqs * max_blocks * 4;
+  if (overlap(k_cache, pool, v_cache, pool) || overlap(out, out_sz, q, q_sz) ||
+      overlap(out, out_sz, k_cache, pool) || overlap(out, out_sz, v_cache, pool) ||
+      overlap(out, out_sz, block_tables, tab_sz) ||
+      overlap(out, out_sz, context_lens, (size_t)num_seqs * 4) ||
+      (need > 0 && (overlap(workspace, need, out, out_sz) || overlap(workspace, need, q, q_sz) ||
+                    overlap(workspace, need, k_cache, pool) ||
+                    overlap(workspace, need, v_cache, pool) ||
+                    overlap(workspace, need, block_tables, tab_sz) ||
+                    overlap(workspace, need, context_lens, (size_t)num_seqs * 4))))
+    return PKV_ERR_ALIAS;
+
+  CUtensorMap kmap, vmap;
+  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    return PKV_ERR_CUDA;
+  unsigned *flags = device_flags();
+  if (!flags) return PKV_ERR_CUDA;
+
+  pkv::DecodeParams p;
+  p.out = out;
+  p.out_dtype = (int)out_dtype;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.max_blocks = max_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.num_gchunks = gchunks;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.part_blocks = part_blocks;
+  p.max_parts = max_parts;
+  p.part_o = need > 0 ? static_cast<float *>(workspace) : nullptr;
+  p.part_ml = need > 0 ? p.part_o + (size_t)num_seqs * num_q_heads * max_parts * head_dim
+                       : nullptr;
+  p.flags = flags;
+
+  int launches = 0;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      dtype == PKV_BF16
+          ? pkv::launch_decode_bf16(kmap, vmap, p, head_dim, block_size, st, &launches)
+          : pkv::launch_decode_f16(kmap, vmap, p, head_dim, block_size, st, &launches);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear, pkv_stream_t stream) {
+  if (!flags_out) return PKV_ERR_NULL;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pkv_flags, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+  *flags_out = v;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_pkv_flags, &zero, sizeof(zero)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

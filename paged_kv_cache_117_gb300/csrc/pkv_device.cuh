@@ -1,0 +1,143 @@
+// Device-side building blocks shared by the paged KV kernels: mbarrier and
+// TMA (cp.async.bulk.tensor) wrappers in inline PTX, 16-bit -> fp32 unpacking
+// and the packed fp32x2 FMA of sm_100-class SMs.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/paged_kv.h"
+
+namespace pkv {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// Spin limit for every mbarrier wait: try_wait suspends for a bounded
+// hardware interval per call, so this bounds a wait to well under a second.
+constexpr uint32_t WAIT_LIMIT = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
+// One 4-D tiled TMA load (box fixed in the tensor map) into shared memory,
+// completing `bytes` on mbarrier `bar`.  Coordinates are innermost first.
+// Out-of-range coordinates read as zeros; nothing outside the tensor is
+// touched.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map,
+                                            int c0, int c1, int c2, int c3,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---- 16-bit -> fp32 --------------------------------------------------------
+// A 32-bit word holds two consecutive 16-bit elements, element 0 in the low
+// half.  bf16 is the top half of an fp32, so widening is a shift or a mask.
+template <typename T>
+struct Widen;
+
+template <>
+struct Widen<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 pair(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+};
+
+template <>
+struct Widen<__half> {
+  static __device__ __forceinline__ float2 pair(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2 *>(&w);
+    return __half22float2(h);
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ float to_float(T x);
+template <>
+__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <>
+__device__ __forceinline__ float to_float<__half>(__half x) {
+  return __half2float(x);
+}
+
+// ---- packed fp32x2 FMA (sm_100 family) -------------------------------------
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  return __ffma2_rn(a, b, c);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// Stores an fp32 value as the requested output dtype.
+__device__ __forceinline__ void store_out(void *base, size_t idx, int out_dtype, float v) {
+  if (out_dtype == PKV_F32) {
+    static_cast<float *>(base)[idx] = v;
+  } else if (out_dtype == PKV_BF16) {
+    static_cast<__nv_bfloat16 *>(base)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half *>(base)[idx] = __float2half_rn(v);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,134 @@
+"""CPU-only checks of the C ABI: the library loads, exports every entry point
+the header declares, and rejects bad arguments on the host before anything
+would be launched (no GPU is touched: every call below fails validation)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_117_gb300 as pkv
+from paged_kv_cache_117_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+OK, NULL, SHAPE, DTYPE, RANGE, ALIAS, CUDA, WS, ALIGN = range(9)
+F16, BF16, F32 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    return pkv.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(", text):
+                if m.group(1) not in ("sizeof", "defined"):
+                    names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(pkv.EXPORTED_SYMBOLS) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.pkv_status_string(code)
+    assert lib.pkv_status_string(99) == b"unknown status"
+
+
+def test_workspace_bytes(lib):
+    # Llama-shaped batch: 256 seqs x 32 heads x 16 partitions x (128 + 2) floats
+    assert lib.paged_attention_workspace_bytes(256, 32, 128, 8192, 512) == 256 * 32 * 16 * 130 * 4
+    assert lib.paged_attention_workspace_bytes(256, 32, 128, 8192, 0) == 0
+    assert lib.paged_attention_workspace_bytes(4, 4, 64, 512, 512) == 0      # one partition
+    assert lib.paged_attention_workspace_bytes(4, 4, 64, 513, 512) == 4 * 4 * 2 * 66 * 4
+    assert lib.paged_attention_workspace_bytes(-1, 4, 64, 512, 16) == ctypes.c_size_t(-1).value
+
+
+P = 1 << 20            # fake, never-dereferenced, 16-byte aligned addresses
+def fake(i): return P * (i + 1)
+
+
+def decode(lib, **kw):
+    a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
+             max_blocks=4, lens=fake(5), S=2, Hq=8, Hkv=2, D=128, B=16, N=8, scale=0.1,
+             pt=0, ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.paged_attention_decode(a["out"], a["out_dt"], a["q"], a["k"], a["v"], a["dt"],
+                                      a["tab"], a["max_blocks"], a["lens"], a["S"], a["Hq"],
+                                      a["Hkv"], a["D"], a["B"], a["N"], a["scale"], a["pt"],
+                                      a["ws"], a["ws_bytes"], None)
+
+
+def test_decode_validation(lib):
+    assert decode(lib, q=None) == NULL
+    assert decode(lib, dt=F32) == DTYPE
+    assert decode(lib, out_dt=7) == DTYPE
+    assert decode(lib, D=96) == SHAPE
+    assert decode(lib, B=12) == SHAPE
+    assert decode(lib, Hq=6, Hkv=4) == SHAPE
+    assert decode(lib, pt=24) == SHAPE
+    assert decode(lib, S=-1) == RANGE
+    assert decode(lib, S=70000) == RANGE
+    assert decode(lib, q=fake(1) + 8) == ALIGN
+    assert decode(lib, k=fake(2), v=fake(2)) == ALIAS
+    assert decode(lib, out=fake(1)) == ALIAS
+    assert decode(lib, pt=16, max_blocks=4) == WS
+    assert decode(lib, pt=16, max_blocks=4, ws=fake(6), ws_bytes=10) == WS
+    assert decode(lib, S=0) == OK           # nothing to do: returns before any CUDA call
+
+
+def test_write_validation(lib):
+    f = lib.paged_kv_write
+    assert f(None, fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 128, BF16, None) == NULL
+    assert f(fake(0), fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 128, F32, None) == DTYPE
+    assert f(fake(0), fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 100, BF16, None) == SHAPE
+    assert f(fake(0), fake(1), fake(2), fake(3), fake(4), -1, 8, 16, 2, 128, BF16, None) == RANGE
+    assert f(fake(0) + 4, fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 128, BF16, None) == ALIGN
+    assert f(fake(0), fake(1), fake(2), fake(2), fake(4), 4, 8, 16, 2, 128, BF16, None) == ALIAS
+    assert f(fake(0), fake(1), fake(2), fake(3), fake(4), 0, 8, 16, 2, 128, BF16, None) == OK
+
+
+def test_copy_validation(lib):
+    f = lib.paged_block_copy
+    assert f(None, fake(1), fake(2), 3, 8, 16, 2, 128, BF16, None) == NULL
+    assert f(fake(0), fake(1), fake(2), 3, 8, 16, 2, 128, 5, None) == DTYPE
+    assert f(fake(0), fake(1), fake(2), 3, 8, 20, 2, 128, BF16, None) == SHAPE
+    assert f(fake(0), fake(1), fake(2), -3, 8, 16, 2, 128, BF16, None) == RANGE
+    assert f(fake(0), fake(1), fake(2) + 4, 3, 8, 16, 2, 128, BF16, None) == ALIGN
+    assert f(fake(0), fake(0), fake(2), 3, 8, 16, 2, 128, BF16, None) == ALIAS
+    assert f(fake(0), fake(1), fake(2), 0, 8, 16, 2, 128, BF16, None) == OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="CUDA library not found"):
+        pkv.load(str(tmp_path / "missing.so"))
+
+
+def test_decode_slot_mapping_matches_oracle_manager():
+    import torch
+    from oracle.block_manager import BlockManager
+    from paged_kv_cache_117_gb300 import workloads as wl
+    bm = BlockManager(64, 4, free_order=wl.free_block_order(wl.TINY))
+    want = []
+    for s, L in enumerate([1, 6, 9, 17]):
+        bm.add_sequence(s)
+        bm.append_tokens(s, L - 1)
+        want.append(bm.append(s)[0])
+    tables = wl.pad_tables([bm.tables[s] for s in range(4)])
+    lens = torch.tensor([1, 6, 9, 17], dtype=torch.int32)
+    got = pkv.decode_slot_mapping(tables, lens, 4)
+    assert got.tolist() == want
+    assert pkv.decode_slot_mapping(tables, torch.tensor([0, 6, 9, 17], dtype=torch.int32), 4)[0] == -1
