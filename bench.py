@@ -65,24 +65,21 @@ def build_metadata(w):
 def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0):
     """Bytes the step must move at minimum: every valid K/V row of every
     (sequence, KV head) once, q, the used block-table entries, lengths, the
-    output, the split-context records (written and read back once), the new
-    K/V rows in and out, and the copied blocks."""
+    output, the split-context records (written once and read back once), the
+    new K/V rows in and out, and the copied blocks."""
     es = w.elem_bytes
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     part_blocks = width if pt == 0 else pt // B
     nb = [-(-L // B) for L in lens]
     nparts = [-(-n // part_blocks) if n else 0 for n in nb]
-    multi = [p for p in nparts if p > 1]
     kv = sum(lens) * Hkv * D * es * 2
-    rec = sum(multi) * Hq * (D + 2) * 4
-    decode = (kv + S * Hq * D * es + sum(nb) * 4 + S * 4
-              + (S - len(multi)) * Hq * D * out_es + rec)
-    merge = rec + len(multi) * Hq * D * out_es + (S * 4 if multi or part_blocks < width else 0)
+    rec = sum(p for p in nparts if p > 1) * Hq * (D + 2) * 4
+    attention = kv + S * Hq * D * es + sum(nb) * 4 + S * 4 + S * Hq * D * out_es + 2 * rec
     write = S * Hkv * D * es * 2 * 2 + S * 8
     block_bytes = B * Hkv * D * es
     copy = n_pairs * block_bytes * 2 * 2 + n_pairs * 16
-    return {"kv": kv, "decode": decode, "merge": merge, "write": write, "copy": copy,
-            "attention": decode + merge, "step": decode + merge + write + copy}
+    return {"kv": kv, "attention": attention, "records": 2 * rec, "write": write,
+            "copy": copy, "step": attention + write + copy}
 
 
 def peak_hbm():
@@ -242,8 +239,8 @@ def run_native(a, world, rank, local):
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0])
-    max_parts = -(-width // (width if pt == 0 else pt // w.block_size))
-    launches_per_step = (1 if pairs.shape[0] else 0) + 1 + 1 + (1 if max_parts > 1 else 0)
+    # block copy (when there are pairs) + KV write + work list + attention
+    launches_per_step = (1 if pairs.shape[0] else 0) + 1 + 2
 
     # CPU-oracle sample: inputs snapshot before any library kernel runs
     cpu = None
@@ -341,7 +338,7 @@ def run_native(a, world, rank, local):
         "seq_steps_per_s": round(world * w.num_seqs / (step_ms * 1e-3), 1),
         "attention_ms": round(dec_ms, 4),
         "bytes_per_step": nbytes,
-        "roofline": {"kernel": "paged_attention_decode (partitioned pass + merge)",
+        "roofline": {"kernel": "paged_attention_decode (work list + attention with fused merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None},

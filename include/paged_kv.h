@@ -23,7 +23,7 @@
  * --------------------------------
  *  - All tensor pointers are DEVICE pointers, owned by the caller, dense
  *    (row-major, no padding) and 16-byte aligned.  The library allocates no
- *    memory: scratch for the split-context pass is passed in (see
+ *    memory: scratch for the attention pass is passed in (see
  *    paged_attention_workspace_bytes).
  *  - Pool layout: k_cache and v_cache are [num_blocks, block_size,
  *    num_kv_heads, head_dim] of the cache dtype.  Slot s of the pool is
@@ -63,7 +63,7 @@ typedef enum {
   PKV_ERR_ALIAS = 5,     /* buffers that must be distinct overlap */
   PKV_ERR_CUDA = 6,      /* a CUDA runtime / driver call failed */
   PKV_ERR_WORKSPACE = 7, /* workspace missing or too small */
-  PKV_ERR_ALIGN = 8      /* a pointer is not 16-byte aligned */
+  PKV_ERR_ALIGN = 8      /* a pointer is not aligned as required */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
@@ -141,16 +141,21 @@ pkv_status paged_block_copy(void *k_cache, void *v_cache,
  *                  block_size] is clamped and flagged (PKV_FLAG_LEN_RANGE)
  *   scale          softmax scale, normally 1/sqrt(head_dim)
  *   partition_tokens
- *                  0: one pass per sequence.  Otherwise a multiple of
+ *                  0: one partition per sequence.  Otherwise a multiple of
  *                  block_size: each sequence's context is cut into partitions
- *                  of this many tokens, processed in parallel, and merged by a
- *                  second launch that rescales by each partition's running
- *                  max (log-sum-exp merge).
- *   workspace      device scratch of at least
+ *                  of this many tokens, processed in parallel; the CTA that
+ *                  finishes a sequence's last partition merges the partition
+ *                  results, rescaling each by its running max (log-sum-exp
+ *                  merge, unnormalised records).
+ *   workspace      device scratch, 256-byte aligned, of at least
  *                  paged_attention_workspace_bytes(num_seqs, num_q_heads,
  *                  head_dim, max_blocks * block_size, partition_tokens)
- *                  bytes; may be NULL when that is 0.  Contents on entry do
- *                  not matter.
+ *                  bytes.  Contents on entry do not matter; the call leaves
+ *                  its work list and partition records there.  Two calls
+ *                  that share a workspace must not overlap in time.
+ *
+ * Two launches: a one-CTA pass that lists the (sequence, partition) work
+ * items in the workspace, then the persistent attention pass.
  */
 pkv_status paged_attention_decode(
     void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
@@ -161,12 +166,16 @@ pkv_status paged_attention_decode(
     size_t workspace_bytes, pkv_stream_t stream);
 
 /*
- * Scratch bytes paged_attention_decode needs: one (max, sum, head_dim-wide
- * unnormalised output) record in fp32 per (sequence, query head, partition),
- * for ceil(max_context / partition_tokens) partitions.  max_context is the
- * capacity of one block-table row (max_blocks * block_size).  Returns 0 when
- * partition_tokens is 0 or at most one partition fits; returns (size_t)-1 on
- * invalid arguments.
+ * Scratch bytes paged_attention_decode needs, with
+ * P = ceil(max_context / partition_tokens) (P = 1 when partition_tokens is 0)
+ * and max_context the capacity of one block-table row (max_blocks *
+ * block_size), each part rounded up to 256 bytes:
+ *   256 (control words) + 4 * num_seqs * num_q_heads (completion counters)
+ *   + 8 * num_seqs * P (work list)
+ *   + when P > 1: 4 * num_seqs * num_q_heads * P * (head_dim + 2)
+ *     (one fp32 (max, sum, unnormalised output) record per sequence, query
+ *     head and partition).
+ * Returns (size_t)-1 on invalid arguments.
  */
 size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
                                        int head_dim, int max_context,
@@ -182,6 +191,13 @@ const char *pkv_status_string(pkv_status status);
  */
 pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear,
                                  pkv_stream_t stream);
+
+/*
+ * Text of the CUDA error behind the last PKV_ERR_CUDA returned on the calling
+ * thread (error name, message and the step that failed); "no error" before
+ * any.  Static per-thread storage, valid until the next failing call.
+ */
+const char *pkv_last_error_string(void);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "paged_attention_workspace_bytes",
     "pkv_status_string",
     "pkv_read_device_flags",
+    "pkv_last_error_string",
 )
 
 
@@ -70,6 +71,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci, vp]
     lib.pkv_read_device_flags.restype = ci
+    lib.pkv_last_error_string.argtypes = []
+    lib.pkv_last_error_string.restype = ctypes.c_char_p
     if path is None:
         _lib = lib
     return lib
@@ -77,7 +80,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
 
 def _check(func: str, status: int) -> None:
     if status != 0:
-        raise PkvError(func, status, load().pkv_status_string(status).decode())
+        text = load().pkv_status_string(status).decode()
+        if status == 6:
+            text += ": " + load().pkv_last_error_string().decode()
+        raise PkvError(func, status, text)
 
 
 def _stream(stream) -> int:

@@ -1,6 +1,7 @@
 // The library's C ABI (declared in include/paged_kv.h): host-side argument
 // checks, TMA descriptor encoding for the pool, and the kernel launches.
 #include <limits.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <mutex>
@@ -76,7 +77,8 @@ bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, in
   const cuuint64_t es = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)B, (cuuint64_t)N};
   cuuint64_t strides[3] = {D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)B * Hkv * D * es};
-  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)B, 1u};
+  // one box = one chunk of up to 16 tokens of one KV head
+  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)(B < 16 ? B : 16), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
@@ -90,6 +92,20 @@ bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, in
   next = (next + 1) & 3;
   *out = map;
   return true;
+}
+
+// Text of the CUDA error behind the last PKV_ERR_CUDA returned on this thread.
+thread_local char g_last_error[256] = "no error";
+
+pkv_status cuda_fail(cudaError_t e, const char *where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return PKV_ERR_CUDA;
+}
+
+pkv_status cuda_fail_msg(const char *msg) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+  return PKV_ERR_CUDA;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -122,7 +138,7 @@ const char *pkv_status_string(pkv_status s) {
     case PKV_ERR_ALIAS: return "buffers overlap";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
-    case PKV_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case PKV_ERR_ALIGN: return "pointer not aligned as required";
   }
   return "unknown status";
 }
@@ -132,11 +148,8 @@ size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_d
   if (num_seqs < 0 || num_q_heads < 0 || head_dim <= 0 || max_context < 0 ||
       partition_tokens < 0)
     return (size_t)-1;
-  if (partition_tokens == 0) return 0;
-  const long long parts = ceil_div_ll(max_context, partition_tokens);
-  if (parts <= 1) return 0;
-  return (size_t)num_seqs * (size_t)num_q_heads * (size_t)parts * (size_t)(head_dim + 2) *
-         sizeof(float);
+  return pkv::workspace_layout(num_seqs, num_q_heads, head_dim, max_context, partition_tokens)
+      .total;
 }
 
 pkv_status paged_kv_write(const void *key, const void *value, void *k_cache, void *v_cache,
@@ -160,12 +173,12 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache, voi
     return PKV_ERR_ALIAS;
   if (row > (size_t)INT_MAX) return PKV_ERR_RANGE;
   unsigned *flags = device_flags();
-  if (!flags) return PKV_ERR_CUDA;
+  if (!flags) return cuda_fail_msg("device flag word unavailable");
   const cudaError_t e = pkv::launch_kv_write(key, value, k_cache, v_cache, slot_mapping,
                                              num_tokens, (int)row,
                                              (long long)num_blocks * block_size, flags,
                                              reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_kv_write launch");
 }
 
 pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_pairs,
@@ -185,11 +198,11 @@ pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_p
       overlap(block_pairs, (size_t)num_pairs * 16, v_cache, pool))
     return PKV_ERR_ALIAS;
   unsigned *flags = device_flags();
-  if (!flags) return PKV_ERR_CUDA;
+  if (!flags) return cuda_fail_msg("device flag word unavailable");
   const cudaError_t e =
       pkv::launch_block_copy(k_cache, v_cache, block_pairs, num_pairs, (long long)block_bytes,
                              num_blocks, flags, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_block_copy launch");
 }
 
 pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
@@ -222,14 +235,13 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
     return PKV_ERR_ALIGN;
 
   const int part_blocks = partition_tokens == 0 ? max_blocks : partition_tokens / block_size;
-  const int max_parts = (int)ceil_div_ll(max_blocks, part_blocks);
-  const size_t need = paged_attention_workspace_bytes(
-      num_seqs, num_q_heads, head_dim, max_blocks * block_size, partition_tokens);
-  if (need == (size_t)-1) return PKV_ERR_RANGE;
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
-    if (!aligned(workspace, 16)) return PKV_ERR_ALIGN;
-  }
+  const pkv::WorkspaceLayout lay = pkv::workspace_layout(
+      num_seqs, num_q_heads, head_dim, (long long)max_blocks * block_size, partition_tokens);
+  const int max_parts = lay.max_parts;
+  if (max_parts != (int)ceil_div_ll(max_blocks, part_blocks)) return PKV_ERR_RANGE;
+  const size_t need = lay.total;
+  if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
 
   const size_t pool = (size_t)num_blocks * block_size * num_kv_heads * head_dim * 2;
   const size_t out_sz = (size_t)num_seqs * num_q_heads * head_dim * dtype_bytes(out_dtype);
@@ -239,19 +251,18 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
       overlap(out, out_sz, k_cache, pool) || overlap(out, out_sz, v_cache, pool) ||
       overlap(out, out_sz, block_tables, tab_sz) ||
       overlap(out, out_sz, context_lens, (size_t)num_seqs * 4) ||
-      (need > 0 && (overlap(workspace, need, out, out_sz) || overlap(workspace, need, q, q_sz) ||
-                    overlap(workspace, need, k_cache, pool) ||
-                    overlap(workspace, need, v_cache, pool) ||
-                    overlap(workspace, need, block_tables, tab_sz) ||
-                    overlap(workspace, need, context_lens, (size_t)num_seqs * 4))))
+      overlap(workspace, need, out, out_sz) || overlap(workspace, need, q, q_sz) ||
+      overlap(workspace, need, k_cache, pool) || overlap(workspace, need, v_cache, pool) ||
+      overlap(workspace, need, block_tables, tab_sz) ||
+      overlap(workspace, need, context_lens, (size_t)num_seqs * 4))
     return PKV_ERR_ALIAS;
 
   CUtensorMap kmap, vmap;
   if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
       !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
-    return PKV_ERR_CUDA;
+    return cuda_fail_msg("cuTensorMapEncodeTiled failed for the KV pool");
   unsigned *flags = device_flags();
-  if (!flags) return PKV_ERR_CUDA;
+  if (!flags) return cuda_fail_msg("device flag word unavailable");
 
   pkv::DecodeParams p;
   p.out = out;
@@ -265,13 +276,19 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   p.num_kv_heads = num_kv_heads;
   p.group = group;
   p.num_gchunks = gchunks;
+  p.num_hc = num_kv_heads * gchunks;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.part_blocks = part_blocks;
   p.max_parts = max_parts;
-  p.part_o = need > 0 ? static_cast<float *>(workspace) : nullptr;
-  p.part_ml = need > 0 ? p.part_o + (size_t)num_seqs * num_q_heads * max_parts * head_dim
-                       : nullptr;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  p.ctrl = reinterpret_cast<unsigned *>(ws + lay.ctrl);
+  p.seq_done = reinterpret_cast<unsigned *>(ws + lay.seq_done);
+  p.items = reinterpret_cast<int2 *>(ws + lay.items);
+  p.part_o = max_parts > 1 ? reinterpret_cast<float *>(ws + lay.part_o) : nullptr;
+  p.part_ml = max_parts > 1 ? reinterpret_cast<float *>(ws + lay.part_ml) : nullptr;
   p.flags = flags;
 
   int launches = 0;
@@ -280,22 +297,25 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
       dtype == PKV_BF16
           ? pkv::launch_decode_bf16(kmap, vmap, p, head_dim, block_size, st, &launches)
           : pkv::launch_decode_f16(kmap, vmap, p, head_dim, block_size, st, &launches);
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention_decode launch");
 }
 
 pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear, pkv_stream_t stream) {
   if (!flags_out) return PKV_ERR_NULL;
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
   unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_pkv_flags, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+  e = cudaMemcpyFromSymbol(&v, g_pkv_flags, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read flag word");
   *flags_out = v;
   if (clear) {
     const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_pkv_flags, &zero, sizeof(zero)) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    e = cudaMemcpyToSymbol(g_pkv_flags, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear flag word");
   }
   return PKV_OK;
 }
+
+const char *pkv_last_error_string(void) { return g_last_error; }
 
 }  // extern "C"

@@ -127,7 +127,12 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return __ffma2_rn(a, b, c);
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x with the SFU's approximate exp2 (relative error about 2^-22); -inf -> +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Stores an fp32 value as the requested output dtype.
 __device__ __forceinline__ void store_out(void *base, size_t idx, int out_dtype, float v) {

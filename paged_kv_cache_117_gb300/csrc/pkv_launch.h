@@ -9,6 +9,38 @@
 
 namespace pkv {
 
+// Workspace carve-up of paged_attention_decode (offsets in bytes, each
+// 256-byte aligned): control words, per-sequence completion counters, the
+// work list, then the partition records when a sequence can span more than
+// one partition.
+struct WorkspaceLayout {
+  size_t ctrl, seq_done, items, part_o, part_ml, total;
+  int max_parts;
+};
+
+inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+inline WorkspaceLayout workspace_layout(long long S, long long Hq, long long D,
+                                        long long max_context, long long partition_tokens) {
+  WorkspaceLayout w{};
+  long long parts = 1;
+  if (partition_tokens > 0) parts = (max_context + partition_tokens - 1) / partition_tokens;
+  if (parts < 1) parts = 1;
+  w.max_parts = (int)parts;
+  w.ctrl = 0;
+  w.seq_done = 256;
+  w.items = w.seq_done + round256((size_t)(S * Hq) * 4);
+  w.part_o = w.items + round256((size_t)(S * parts) * 8);
+  if (parts > 1) {
+    w.part_ml = w.part_o + (size_t)(S * Hq * parts * D) * 4;
+    w.total = w.part_ml + (size_t)(S * Hq * parts) * 8;
+  } else {
+    w.part_ml = w.part_o;
+    w.total = w.part_o;
+  }
+  return w;
+}
+
 struct DecodeParams {
   void *out;
   int out_dtype;                 // pkv_dtype
@@ -20,18 +52,24 @@ struct DecodeParams {
   int num_q_heads;
   int num_kv_heads;
   int group;                     // Hq / Hkv
-  int num_gchunks;               // CTAs per KV head along the query group
+  int num_gchunks;               // query-head chunks (<= 8 heads) per KV head
+  int num_hc;                    // num_kv_heads * num_gchunks
+  int head_dim;
+  int block_size;
   int num_blocks;                // pool size, for range checks
   float scale_log2;              // scale * log2(e): scores live in the exp2 domain
   int part_blocks;               // blocks per partition
   int max_parts;                 // partitions per sequence the workspace holds
   float *part_ml;                // [S, Hq, max_parts, 2]  (running max, sum)
   float *part_o;                 // [S, Hq, max_parts, D]  unnormalised output
+  unsigned *ctrl;                // [0] next work unit, [1] number of work units
+  unsigned *seq_done;            // [S, num_hc] partitions finished per sequence
+  int2 *items;                   // [S * max_parts] (sequence, partition) work list
   unsigned *flags;               // device flag word
 };
 
-// Launch the decode pass (and, when max_parts > 1, the merge pass) for one
-// cache dtype / head_dim / block_size combination.  Returns a cudaError_t.
+// Launch the work-list pass and the decode pass for one cache dtype /
+// head_dim / block_size combination.  Returns a cudaError_t.
 cudaError_t launch_decode_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                const DecodeParams &p, int head_dim, int block_size,
                                cudaStream_t stream, int *launches);

@@ -48,12 +48,20 @@ def test_status_strings(lib):
     assert lib.pkv_status_string(99) == b"unknown status"
 
 
+def _expected_ws(S, Hq, D, ctx, pt):
+    r = lambda x: -(-x // 256) * 256
+    P = 1 if pt == 0 else max(1, -(-ctx // pt))
+    n = 256 + r(4 * S * Hq) + r(8 * S * P)
+    return n + (4 * S * Hq * P * (D + 2) if P > 1 else 0)
+
+
 def test_workspace_bytes(lib):
-    # Llama-shaped batch: 256 seqs x 32 heads x 16 partitions x (128 + 2) floats
-    assert lib.paged_attention_workspace_bytes(256, 32, 128, 8192, 512) == 256 * 32 * 16 * 130 * 4
-    assert lib.paged_attention_workspace_bytes(256, 32, 128, 8192, 0) == 0
-    assert lib.paged_attention_workspace_bytes(4, 4, 64, 512, 512) == 0      # one partition
-    assert lib.paged_attention_workspace_bytes(4, 4, 64, 513, 512) == 4 * 4 * 2 * 66 * 4
+    # Llama-shaped batch: 256 seqs x 32 heads x 16 partitions x (128 + 2) floats + control
+    assert lib.paged_attention_workspace_bytes(256, 32, 128, 8192, 512) == \
+        256 + 256 * 32 * 4 + 256 * 16 * 8 + 256 * 32 * 16 * 130 * 4
+    for args in [(256, 32, 128, 8192, 0), (4, 4, 64, 512, 512), (4, 4, 64, 513, 512),
+                 (3, 5, 128, 100, 16), (1, 1, 64, 16, 16)]:
+        assert lib.paged_attention_workspace_bytes(*args) == _expected_ws(*args), args
     assert lib.paged_attention_workspace_bytes(-1, 4, 64, 512, 16) == ctypes.c_size_t(-1).value
 
 
@@ -64,7 +72,7 @@ def fake(i): return P * (i + 1)
 def decode(lib, **kw):
     a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
              max_blocks=4, lens=fake(5), S=2, Hq=8, Hkv=2, D=128, B=16, N=8, scale=0.1,
-             pt=0, ws=None, ws_bytes=0)
+             pt=0, ws=fake(6), ws_bytes=1 << 20)
     a.update(kw)
     return lib.paged_attention_decode(a["out"], a["out_dt"], a["q"], a["k"], a["v"], a["dt"],
                                       a["tab"], a["max_blocks"], a["lens"], a["S"], a["Hq"],
@@ -85,8 +93,10 @@ def test_decode_validation(lib):
     assert decode(lib, q=fake(1) + 8) == ALIGN
     assert decode(lib, k=fake(2), v=fake(2)) == ALIAS
     assert decode(lib, out=fake(1)) == ALIAS
-    assert decode(lib, pt=16, max_blocks=4) == WS
-    assert decode(lib, pt=16, max_blocks=4, ws=fake(6), ws_bytes=10) == WS
+    assert decode(lib, ws=None) == WS
+    assert decode(lib, ws_bytes=10) == WS
+    assert decode(lib, ws=fake(6) + 16) == ALIGN
+    assert decode(lib, ws=fake(1)) == ALIAS
     assert decode(lib, S=0) == OK           # nothing to do: returns before any CUDA call
 
 
