@@ -48,8 +48,10 @@ unsigned *device_flags() {
   return ptrs[dev];
 }
 
-// TMA descriptor over one pool [N, B, Hkv, D] whose box is one KV head's
-// [B, D] tile of one block.  A few recent descriptors are cached per thread.
+// TMA descriptor over one pool [N, B, Hkv, D] whose box is a [min(B, 16), 64]
+// slab of one KV head of one block, 128B-swizzled in shared memory (the
+// layout the decode kernel's ldmatrix reads assume).  A few recent
+// descriptors are cached per thread.
 struct MapKey {
   const void *base;
   int dt, n, b, h, d;
@@ -77,15 +79,15 @@ bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, in
   const cuuint64_t es = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)B, (cuuint64_t)N};
   cuuint64_t strides[3] = {D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)B * Hkv * D * es};
-  // one box = one chunk of up to 16 tokens of one KV head
-  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)(B < 16 ? B : 16), 1u};
+  // one box = 64 dims (128 bytes, 128B-swizzled) x up to 16 tokens of one KV head
+  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)(B < 16 ? B : 16), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
   const CUtensorMapDataType t =
       dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUresult r = fn(&map, t, 4, const_cast<void *>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   cache[next] = Entry{key, map, true};
@@ -226,7 +228,7 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   if (num_seqs == 0) return PKV_OK;
   if (num_seqs > 65535) return PKV_ERR_RANGE;
   const int group = num_q_heads / num_kv_heads;
-  const int gchunks = group <= 8 ? 1 : (group + 7) / 8;
+  const int gchunks = group <= 16 ? 1 : (group + 15) / 16;
   if ((long long)num_kv_heads * gchunks > 65535) return PKV_ERR_RANGE;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||

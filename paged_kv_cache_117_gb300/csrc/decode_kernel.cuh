@@ -60,103 +60,48 @@ constexpr int round_up_c(int v, int a) { return (v + a - 1) / a * a; }
 
 constexpr int DECODE_WARPS = 4;
 
-// CTAs per SM the kernel is shaped for: 3 when the register budget allows
-// (up to 4 query heads per CTA), otherwise 2.
-constexpr int occupancy_for(int GT) { return GT >= 8 ? 2 : 3; }
+// CTAs per SM the kernel is shaped for: 3 up to 8 query heads per CTA,
+// 2 for 16 (larger merge area).
+constexpr int occupancy_for(int GT) { return GT >= 16 ? 2 : 3; }
 
-// Stages per warp: fill about 220 KiB of shared memory across the CTAs of an
-// SM, 2..4 stages.
+// Stages per warp: fill the shared memory of an SM across its CTAs, 2..4.
 constexpr int stages_for(int stage_bytes, int occ) {
-  return max_c(2, min_c(4, (220 * 1024 / occ - 4096) / (DECODE_WARPS * stage_bytes)));
+  return max_c(2, min_c(4, (227 * 1024 / occ - 3 * 1024) / (DECODE_WARPS * stage_bytes)));
 }
+
+// Softmax reference-max slack (log2 domain): the running maximum used for
+// the exponentials is raised only when a score exceeds it by more than this,
+// so P stays <= 2^8 and the rescale of O is rare.  Exact: O and L always use
+// the same reference.
+constexpr float RESCALE_SLACK = 8.0f;
 
 template <typename T, int D, int B, int GT>
 struct DecodeCfg {
   static constexpr int NW = DECODE_WARPS;
   static constexpr int OCC = occupancy_for(GT);
-  static constexpr int CH = min_c(B, 16);        // tokens per chunk (one TMA box)
+  static constexpr int CH = min_c(B, 16);        // tokens per chunk (one TMA box high)
   static constexpr int NCH = B / CH;             // chunks per block
-  static constexpr int HT = CH / 2;              // tokens per half-warp per chunk
-  static constexpr int DPL = D / 16;             // dims owned by a lane
-  static constexpr int WPL = DPL / 2;            // 32-bit words per lane row slice
-  static constexpr int CHUNK_ELEMS = CH * D;
-  static constexpr int CHUNK_BYTES = CHUNK_ELEMS * (int)sizeof(T);
-  static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;   // K + V
+  static constexpr int NT = (CH + 7) / 8;        // 8-token MMA n-tiles in Q.K^T
+  static constexpr int NSUB = D / 64;            // 128-byte column slabs of a row
+  static constexpr int KS = D / 16;              // k-steps of Q.K^T
+  static constexpr int NTD = D / 8;              // 8-dim MMA n-tiles of P.V
+  static constexpr int SUB_BYTES = 16 * 128;     // one slab: 16 rows x 128 B, 128B-swizzled
+  static constexpr int CHUNK_BYTES = NSUB * SUB_BYTES;   // K (or V) of one chunk
+  static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;    // K + V
+  static constexpr int TX_BYTES = 2 * NSUB * CH * 128;   // bytes the TMA loads deliver
   static constexpr int STAGES = stages_for(STAGE_BYTES, OCC);
-  static constexpr int GP = min_c(GT, 4);        // heads per score pass
-  static constexpr int NPASS = GT / GP;
-  static constexpr int V = HT * GP;              // partial scores per lane per pass
-  static constexpr int LPG = 16 / GP;            // lanes per head within a half-warp
-  static constexpr int SCAT = V >= 16 ? 4 : ilog2_c(V);
-  static constexpr int DUP_BITS = 4 - SCAT;      // lanes holding copies of one sum
-  static constexpr int R = V >= 16 ? V / 16 : 1; // sums owned per lane
   // shared memory (bytes)
   static constexpr int STAGES_BYTES = NW * STAGES * STAGE_BYTES;
   static constexpr int MERGE_BYTES = NW * GT * (D + 2) * 4;
-  static constexpr int BIG_BYTES = round_up_c(max_c(STAGES_BYTES, MERGE_BYTES), 128);
-  static constexpr int P_FLOATS = NW * 2 * HT * GT * 2;   // (p, p) pairs
-  static constexpr int A_FLOATS = NW * GT;
-  static constexpr int SMALL_BYTES = round_up_c((P_FLOATS + A_FLOATS) * 4, 16);
+  static constexpr int BIG_BYTES = round_up_c(max_c(STAGES_BYTES, MERGE_BYTES), 1024);
   static constexpr int BAR_BYTES = NW * STAGES * 8;
-  static constexpr int SMEM_BYTES = 1024 + BIG_BYTES + SMALL_BYTES + BAR_BYTES + 16;
+  static constexpr int SMEM_BYTES = 1024 + BIG_BYTES + BAR_BYTES + 16;
 
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(B == 4 || B == 8 || B == 16 || B == 32, "block_size");
-  static_assert(GT == 1 || GT == 2 || GT == 4 || GT == 8, "query head chunk");
-  static_assert(R <= HT, "a lane's sums belong to one head");
+  static_assert(GT == 1 || GT == 4 || GT == 8 || GT == 16, "query head rows");
   static_assert(SMEM_BYTES * OCC <= 227 * 1024, "shared memory budget");
 };
-
-// Sum v[] over the 16 lanes of each half-warp.  Afterwards lane li holds, in
-// v[0 .. R-1], the full sums of the original entries
-// [(li >> DUP_BITS) * R, ... + R).  Each exchange step sends half of the live
-// entries to the partner lane and keeps the other half.
-template <int V>
-__device__ __forceinline__ void half_reduce_scatter(float (&v)[V], int li) {
-#pragma unroll
-  for (int step = 0; step < 4; ++step) {
-    const int off = 8 >> step;
-    const int n = (V >> step) > 1 ? (V >> step) : 1;
-    if (n > 1) {
-      const int h = n >> 1;
-      const bool upper = (li & off) != 0;
-#pragma unroll
-      for (int k = 0; k < h; ++k) {
-        const float send = upper ? v[k] : v[k + h];
-        const float keep = upper ? v[k + h] : v[k];
-        v[k] = keep + __shfl_xor_sync(FULL_MASK, send, off);
-      }
-    } else {
-      v[0] += __shfl_xor_sync(FULL_MASK, v[0], off);
-    }
-  }
-}
-
-template <int W>
-__device__ __forceinline__ void load_words(const void *p, uint32_t (&w)[W]);
-template <>
-__device__ __forceinline__ void load_words<4>(const void *p, uint32_t (&w)[4]) {
-  const uint4 x = *reinterpret_cast<const uint4 *>(p);
-  w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-}
-template <>
-__device__ __forceinline__ void load_words<2>(const void *p, uint32_t (&w)[2]) {
-  const uint2 x = *reinterpret_cast<const uint2 *>(p);
-  w[0] = x.x; w[1] = x.y;
-}
-
-template <int W>
-__device__ __forceinline__ void ldg_words(const void *p, uint32_t (&w)[W]);
-template <>
-__device__ __forceinline__ void ldg_words<4>(const void *p, uint32_t (&w)[4]) {
-  const uint4 x = __ldg(reinterpret_cast<const uint4 *>(p));
-  w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-}
-template <>
-__device__ __forceinline__ void ldg_words<2>(const void *p, uint32_t (&w)[2]) {
-  const uint2 x = __ldg(reinterpret_cast<const uint2 *>(p));
-  w[0] = x.x; w[1] = x.y;
-}
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
@@ -231,17 +176,21 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  T *stages = reinterpret_cast<T *>(smem);
-  float *p_s = reinterpret_cast<float *>(smem + C::BIG_BYTES);
-  float *a_s = p_s + C::P_FLOATS;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BIG_BYTES + C::SMALL_BYTES);
+  const uint32_t stage_smem = smem_addr(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BIG_BYTES);
   volatile int *s_int = reinterpret_cast<volatile int *>(bars + NW * STAGES);  // next, abort, last
 
   const int tid = threadIdx.x;
-  const int lane = tid & 31, w = tid >> 5, half = lane >> 4, li = lane & 15;
+  const int lane = tid & 31, w = tid >> 5;
   const int HC = p.num_hc;
   const int cap = p.max_blocks * B;
 
+  // Rows a chunk never loads (block_size < 16) must read as zeros in P.V.
+  if (C::CH < 16) {
+    for (int i = tid; i < C::STAGES_BYTES / 16; i += NW * 32)
+      *reinterpret_cast<uint4 *>(smem + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < NW * STAGES; ++i) mbar_init(smem_addr(bars + i), 1);
@@ -256,17 +205,18 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
   const unsigned total = __ldcg(p.ctrl + 1);
   __syncthreads();
 
-  T *wst = stages + (size_t)w * STAGES * 2 * C::CHUNK_ELEMS;
+  const uint32_t wst = stage_smem + w * STAGES * C::STAGE_BYTES;
   const uint32_t bar0 = smem_addr(bars + w * STAGES);
   const uint64_t pol = l2_policy_evict_first();
-  float2 *pw = reinterpret_cast<float2 *>(p_s) + w * (2 * C::HT * GT);
-  float *aw = a_s + w * GT;
   uint32_t ld_cnt = 0, use_cnt = 0;   // this warp's loads issued / consumed, all units
 
-  const int g_loc = li / C::LPG;                      // head within a score pass
-  const int base_idx = (li >> C::DUP_BITS) * C::R;
-  const int tt0 = base_idx - g_loc * C::HT;
-  const bool primary = (li & ((1 << C::DUP_BITS) - 1)) == 0;
+  // fragment coordinates of this lane
+  const int r0 = lane >> 2;                         // C rows r0 and r0 + 8 (query heads)
+  const int cq = 2 * (lane & 3);                    // C columns cq, cq + 1
+  const int k_tok = ((lane >> 4) & 1) * 8 + (lane & 7);   // ldmatrix row for K (B operand)
+  const int k_chb = (lane >> 3) & 1;
+  const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);   // ldmatrix row for V (trans)
+  const int v_chb = (lane >> 4) & 1;
 
   unsigned unit = (unsigned)s_int[0];
 #pragma unroll 1
@@ -313,51 +263,49 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
         if ((unsigned)pb >= (unsigned)p.num_blocks) atomicOr(p.flags, PKV_FLAG_BLOCK_RANGE);
         const int stage = (int)(ld_cnt % STAGES);
         const uint32_t bar = bar0 + stage * 8;
-        T *kdst = wst + stage * 2 * C::CHUNK_ELEMS;
-        mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
+        const uint32_t dst = wst + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(bar, C::TX_BYTES);
         // out-of-range block ids read as zeros (TMA bounds), never fault
-        tma_load_4d(smem_addr(kdst), &kmap, 0, kvh, c * C::CH, pb, bar, pol);
-        tma_load_4d(smem_addr(kdst + C::CHUNK_ELEMS), &vmap, 0, kvh, c * C::CH, pb, bar, pol);
+#pragma unroll
+        for (int sb = 0; sb < C::NSUB; ++sb) {
+          tma_load_4d(dst + sb * C::SUB_BYTES, &kmap, sb * 64, kvh, c * C::CH, pb, bar, pol);
+          tma_load_4d(dst + C::CHUNK_BYTES + sb * C::SUB_BYTES, &vmap, sb * 64, kvh,
+                      c * C::CH, pb, bar, pol);
+        }
       }
       ++ld_cnt;
     };
 
-    // The stage area held the previous unit's merge data (generic-proxy
-    // writes); order those before this unit's TMA writes.  Within a unit a
-    // stage is refilled only after every lane's reads of it have returned.
+    // The stage area held the previous unit's merge data: every thread
+    // fenced its generic writes before the unit barrier; order them ahead of
+    // this unit's TMA writes.  Within a unit a stage is refilled only after
+    // every lane's reads of it have returned.
     if (lane == 0) fence_proxy_async_smem();
     int issued = 0;
     for (; issued < n_units && issued < STAGES; ++issued) issue(issued);
 
-    // ---- query slice in registers, pre-scaled into the exp2 domain --------
-    float2 q2[GT][C::WPL];
+    // ---- query rows as MMA A fragments (rows >= gcount are zero) ----------
+    uint32_t qa[C::KS][4];
     {
-      const T *qb = static_cast<const T *>(p.q) + out_base + li * C::DPL;
+      const T *qb = static_cast<const T *>(p.q) + out_base;
 #pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        uint32_t wv[C::WPL];
-        if (g < gcount) {
-          ldg_words<C::WPL>(qb + g * D, wv);
-        } else {
+      for (int ks = 0; ks < C::KS; ++ks)
 #pragma unroll
-          for (int k = 0; k < C::WPL; ++k) wv[k] = 0u;
+        for (int e = 0; e < 4; ++e) {
+          const int row = r0 + ((e & 1) ? 8 : 0);
+          const int kk = ks * 16 + cq + ((e & 2) ? 8 : 0);
+          qa[ks][e] = row < gcount
+                          ? __ldg(reinterpret_cast<const unsigned int *>(qb + row * D + kk))
+                          : 0u;
         }
-#pragma unroll
-        for (int k = 0; k < C::WPL; ++k) {
-          const float2 f = Widen<T>::pair(wv[k]);
-          q2[g][k] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-        }
-      }
     }
 
-    float m_run[C::NPASS], l_run[C::NPASS];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[C::NTD][4];
 #pragma unroll
-    for (int ps = 0; ps < C::NPASS; ++ps) { m_run[ps] = -INFINITY; l_run[ps] = 0.f; }
-    float2 o2[GT][C::WPL];
+    for (int nt = 0; nt < C::NTD; ++nt)
 #pragma unroll
-    for (int g = 0; g < GT; ++g)
-#pragma unroll
-      for (int k = 0; k < C::WPL; ++k) o2[g][k] = make_float2(0.f, 0.f);
+      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
 
     bool ok = true;
     int u = 0;
@@ -373,100 +321,110 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
       const int c = u - i * C::NCH;
       const int j = j0 + i * NW;
       const int valid = min(C::CH, L - j * B - c * C::CH);   // >= 1
-      const T *kt = wst + stage * 2 * C::CHUNK_ELEMS;
-      const T *vt = kt + C::CHUNK_ELEMS;
+      const uint32_t kb = wst + stage * C::STAGE_BYTES;
+      const uint32_t vb = kb + C::CHUNK_BYTES;
 
-      float alpha_own[C::NPASS];
-#pragma unroll
-      for (int ps = 0; ps < C::NPASS; ++ps) {
-        // scores of this half's tokens against heads ps*GP .. ps*GP+GP-1
-        float sc[C::V];
-#pragma unroll
-        for (int tt = 0; tt < C::HT; ++tt) {
-          const int t = half * C::HT + tt;
-          uint32_t kw[C::WPL];
-          load_words<C::WPL>(kt + t * D + li * C::DPL, kw);
-          float2 kf[C::WPL];
-#pragma unroll
-          for (int k = 0; k < C::WPL; ++k) kf[k] = Widen<T>::pair(kw[k]);
-#pragma unroll
-          for (int gl = 0; gl < C::GP; ++gl) {
-            const int g = ps * C::GP + gl;
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < C::WPL; ++k) acc = fma2(q2[g][k], kf[k], acc);
-            sc[gl * C::HT + tt] = acc.x + acc.y;
-          }
+      if (valid < C::CH) {
+        // rows at or past the context length hold stale pool bytes: zero the
+        // V rows so that 0 * V stays 0 in P.V (K rows are masked below)
+        unsigned char *vrow = smem + (vb - stage_smem);
+        for (int x = lane; x < (C::CH - valid) * C::NSUB * 8; x += 32) {
+          const int piece = x & 7;
+          const int rr = x >> 3;
+          const int sb = rr % C::NSUB;
+          const int row = valid + rr / C::NSUB;
+          *reinterpret_cast<uint4 *>(vrow + sb * C::SUB_BYTES + row * 128 + piece * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
-        half_reduce_scatter<C::V>(sc, li);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
 
-        // online softmax of head ps*GP + g_loc (identical in all lanes of the
-        // group and in both halves)
-        float own[C::R];
-        float bmax = -INFINITY;
+      // S = Q K^T (rows: query heads, columns: the chunk's tokens)
+      float sa[C::NT][4];
 #pragma unroll
-        for (int r = 0; r < C::R; ++r) {
-          const int t = half * C::HT + tt0 + r;
-          own[r] = t < valid ? sc[r] : -INFINITY;
-          bmax = fmaxf(bmax, own[r]);
-        }
+      for (int jn = 0; jn < C::NT; ++jn)
 #pragma unroll
-        for (int off = 1; off < C::LPG; off <<= 1)
-          bmax = fmaxf(bmax, __shfl_xor_sync(FULL_MASK, bmax, off));
-        bmax = fmaxf(bmax, __shfl_xor_sync(FULL_MASK, bmax, 16));
-        const float m_new = fmaxf(m_run[ps], bmax);
-        const float alpha = fast_exp2(m_run[ps] - m_new);
-        float lsum = 0.f;
+        for (int e = 0; e < 4; ++e) sa[jn][e] = 0.f;
 #pragma unroll
-        for (int r = 0; r < C::R; ++r) {
-          own[r] = fast_exp2(own[r] - m_new);
-          lsum += own[r];
-        }
-        if (!primary) lsum = 0.f;
-#pragma unroll
-        for (int off = 1; off < C::LPG; off <<= 1)
-          lsum += __shfl_xor_sync(FULL_MASK, lsum, off);
-        lsum += __shfl_xor_sync(FULL_MASK, lsum, 16);
-        l_run[ps] = l_run[ps] * alpha + lsum;
-        m_run[ps] = m_new;
-        alpha_own[ps] = alpha;
-        if (primary) {
-#pragma unroll
-          for (int r = 0; r < C::R; ++r)
-            pw[(half * C::HT + tt0 + r) * GT + ps * C::GP + g_loc] = make_float2(own[r], own[r]);
+      for (int ks = 0; ks < C::KS; ++ks) {
+        const int sb = ks >> 2;
+        const int ch = (ks & 3) * 2 + k_chb;
+        const uint32_t addr = kb + sb * C::SUB_BYTES + k_tok * 128 + ((ch ^ (k_tok & 7)) << 4);
+        if (C::NT == 2) {
+          uint32_t r[4];
+          ldsm_x4(r, addr);
+          Mma<T>::run(sa[0], qa[ks], r[0], r[1]);
+          Mma<T>::run(sa[C::NT - 1], qa[ks], r[2], r[3]);
+        } else {
+          uint32_t r[2];
+          ldsm_x2(r, addr);
+          Mma<T>::run(sa[0], qa[ks], r[0], r[1]);
         }
       }
-      if (half == 0 && (li % C::LPG) == 0) {
-#pragma unroll
-        for (int ps = 0; ps < C::NPASS; ++ps) aw[ps * C::GP + g_loc] = alpha_own[ps];
-      }
-      __syncwarp();
 
+      // online softmax (exp2 domain) with a lazily raised reference max
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        const float a = aw[g];
-        const float2 aa = make_float2(a, a);
+      for (int jn = 0; jn < C::NT; ++jn)
 #pragma unroll
-        for (int k = 0; k < C::WPL; ++k) o2[g][k] = __fmul2_rn(o2[g][k], aa);
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int tok = 8 * jn + cq + (e & 1);
+          const float x = tok < valid ? sa[jn][e] * p.scale_log2 : -INFINITY;
+          sa[jn][e] = x;
+          if (e < 2) mx0 = fmaxf(mx0, x); else mx1 = fmaxf(mx1, x);
+        }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
+      const bool up0 = mx0 > m0 + RESCALE_SLACK, up1 = mx1 > m1 + RESCALE_SLACK;
+      if (__any_sync(FULL_MASK, up0 || up1)) {
+        const float n0 = up0 ? mx0 : m0, n1 = up1 ? mx1 : m1;
+        const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
 #pragma unroll
-      for (int tt = 0; tt < C::HT; ++tt) {
-        const int t = half * C::HT + tt;
-        uint32_t vw[C::WPL];
-        load_words<C::WPL>(vt + t * D + li * C::DPL, vw);
-        float2 pp[GT];
-#pragma unroll
-        for (int g = 0; g < GT; ++g) pp[g] = pw[(half * C::HT + tt) * GT + g];
-        if (t < valid) {
-#pragma unroll
-          for (int k = 0; k < C::WPL; ++k) {
-            const float2 vf = Widen<T>::pair(vw[k]);
-#pragma unroll
-            for (int g = 0; g < GT; ++g) o2[g][k] = fma2(pp[g], vf, o2[g][k]);
-          }
+        for (int nt = 0; nt < C::NTD; ++nt) {
+          o[nt][0] *= a0; o[nt][1] *= a0;
+          o[nt][2] *= a1; o[nt][3] *= a1;
         }
       }
-      __syncwarp();   // P / alpha and this stage's K, V reads are done
+      uint32_t ah[4], al[4];
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn) {
+        if (jn < C::NT) {
+          const float p00 = fast_exp2(sa[jn][0] - m0), p01 = fast_exp2(sa[jn][1] - m0);
+          const float p10 = fast_exp2(sa[jn][2] - m1), p11 = fast_exp2(sa[jn][3] - m1);
+          l0 += p00 + p01;
+          l1 += p10 + p11;
+          // P in two 16-bit pieces (hi + lo) keeps about 16 mantissa bits
+          const uint32_t h0 = Mma<T>::pack(p00, p01), h1 = Mma<T>::pack(p10, p11);
+          const float2 b0 = Widen<T>::pair(h0), b1 = Widen<T>::pair(h1);
+          ah[2 * jn + 0] = h0;
+          ah[2 * jn + 1] = h1;
+          al[2 * jn + 0] = Mma<T>::pack(p00 - b0.x, p01 - b0.y);
+          al[2 * jn + 1] = Mma<T>::pack(p10 - b1.x, p11 - b1.y);
+        } else {
+          ah[2 * jn] = ah[2 * jn + 1] = al[2 * jn] = al[2 * jn + 1] = 0u;
+        }
+      }
+
+      // O += P V
+#pragma unroll
+      for (int nt = 0; nt < C::NTD; nt += 2) {
+        const int sb = nt >> 3;
+        const int ch = (nt & 7) + v_chb;
+        uint32_t r[4];
+        ldsm_x4_trans(r, vb + sb * C::SUB_BYTES + v_tok * 128 + ((ch ^ (v_tok & 7)) << 4));
+        Mma<T>::run(o[nt], ah, r[0], r[1]);
+        Mma<T>::run(o[nt], al, r[0], r[1]);
+        Mma<T>::run(o[nt + 1], ah, r[2], r[3]);
+        Mma<T>::run(o[nt + 1], al, r[2], r[3]);
+      }
+      __syncwarp();   // every lane's reads of this stage have returned
       ++use_cnt;
       if (issued < n_units) {
         issue(issued);
@@ -484,29 +442,26 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
         (void)mbar_wait_bounded(bar0 + (use_cnt % STAGES) * 8, (use_cnt / STAGES) & 1u);
     }
 
-    // both halves accumulated different tokens of the same heads and dims
-#pragma unroll
-    for (int g = 0; g < GT; ++g)
-#pragma unroll
-      for (int k = 0; k < C::WPL; ++k) {
-        o2[g][k].x += __shfl_xor_sync(FULL_MASK, o2[g][k].x, 16);
-        o2[g][k].y += __shfl_xor_sync(FULL_MASK, o2[g][k].y, 16);
-      }
+    // row sums: the 4 lanes of a row hold different columns
+    l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
+    l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
+    l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
+    l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
 
     __syncthreads();  // every stage consumed: the stage area becomes merge space
     float *mg_o = reinterpret_cast<float *>(smem);    // [NW][GT][D]
     float *mg_ml = mg_o + NW * GT * D;                 // [NW][GT][2]
-    if (half == 0) {
 #pragma unroll
-      for (int g = 0; g < GT; ++g)
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = r0 + 8 * hr;
+      if (row < gcount) {
 #pragma unroll
-        for (int k = 0; k < C::WPL; ++k)
-          *reinterpret_cast<float2 *>(mg_o + (w * GT + g) * D + li * C::DPL + 2 * k) = o2[g][k];
-      if (li % C::LPG == 0) {
-#pragma unroll
-        for (int ps = 0; ps < C::NPASS; ++ps) {
-          mg_ml[(w * GT + ps * C::GP + g_loc) * 2 + 0] = m_run[ps];
-          mg_ml[(w * GT + ps * C::GP + g_loc) * 2 + 1] = l_run[ps];
+        for (int nt = 0; nt < C::NTD; ++nt)
+          *reinterpret_cast<float2 *>(mg_o + (w * GT + row) * D + 8 * nt + cq) =
+              make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
+        if ((lane & 3) == 0) {
+          mg_ml[(w * GT + row) * 2 + 0] = hr ? m1 : m0;
+          mg_ml[(w * GT + row) * 2 + 1] = hr ? l1 : l0;
         }
       }
     }
@@ -568,7 +523,13 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
         }
       }
     }
-    __syncthreads();  // merge space is free again; s_int[0] holds the next unit
+    __syncthreads();  // merge reads done
+    if (C::CH < 16) {   // the merge overwrote rows that must stay zero
+      for (int i2 = tid; i2 < C::MERGE_BYTES / 16; i2 += NW * 32)
+        *reinterpret_cast<uint4 *>(smem + i2 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();  // stage area free again; s_int[0] holds the next unit
     if (abort) break;
     unit = (unsigned)s_int[0];
   }
@@ -642,11 +603,11 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
 template <typename T, int D, int B>
 cudaError_t launch_decode_gt(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, cudaStream_t stream, int *launches) {
-  const int g = p.group >= 8 ? 8 : p.group;
+  const int g = p.group >= 16 ? 16 : p.group;
   if (g <= 1) return launch_decode_cfg<T, D, B, 1>(kmap, vmap, p, stream, launches);
-  if (g <= 2) return launch_decode_cfg<T, D, B, 2>(kmap, vmap, p, stream, launches);
   if (g <= 4) return launch_decode_cfg<T, D, B, 4>(kmap, vmap, p, stream, launches);
-  return launch_decode_cfg<T, D, B, 8>(kmap, vmap, p, stream, launches);
+  if (g <= 8) return launch_decode_cfg<T, D, B, 8>(kmap, vmap, p, stream, launches);
+  return launch_decode_cfg<T, D, B, 16>(kmap, vmap, p, stream, launches);
 }
 
 template <typename T, int D>

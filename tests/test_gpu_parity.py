@@ -107,7 +107,7 @@ def test_boundary_lengths(pt):
     err, plan = run_full_compare(w, width=130)
 
 
-@pytest.mark.parametrize("hq,hkv", [(3, 1), (12, 2), (16, 1), (24, 2), (5, 5), (8, 8), (32, 4)])
+@pytest.mark.parametrize("hq,hkv", [(3, 1), (12, 2), (16, 1), (24, 2), (5, 5), (8, 8), (32, 4), (40, 2), (64, 2)])
 def test_group_sizes(hq, hkv):
     w = _custom("groups", [3, 40, 129, 300], hq, hkv, 64, 8, pt=64)
     run_full_compare(w)
