@@ -9,39 +9,43 @@
 // group of its KV head.
 //
 // Work decomposition.  A sequence's context is cut into partitions of
-// part_blocks blocks.  A work unit is (sequence, partition, KV head, query
-// head chunk of <= 8).  decode_plan_kernel (one CTA) lists the (sequence,
+// part_blocks blocks.  A work unit is (sequence, partition, KV head, chunk of
+// up to 16 query heads).  decode_plan_kernel (one CTA) lists the (sequence,
 // partition) items in the workspace -- all full partitions first, then the
 // shorter last partitions -- and resets the work counter and the per-sequence
 // completion counters.  decode_kernel runs as a persistent grid sized to fill
-// the SMs; each CTA takes the next unit with one atomicAdd (fetched while the
-// current unit is processed), so no CTA slot is spent on empty work and the
-// short units land at the end.
+// the SMs; each CTA takes units with atomicAdd, two ahead of the one it is
+// processing, so that every warp knows its next unit while it works on the
+// current one.
 //
-// Inside a CTA (4 warps), warp w streams blocks jb + w, jb + w + 4, ... of the
-// partition through a private ring of STAGES shared-memory stages.  One lane
-// issues two 4-D TMA tile loads per chunk of <= 16 tokens (K and V tile
-// [chunk, head_dim] of one KV head; pool layout [N, B, Hkv, D], so a tile is
-// `chunk` rows of head_dim*2 bytes at a stride of Hkv*head_dim*2 bytes),
-// completing on the stage's mbarrier; the stage/phase counters run on across
-// units, so barriers are initialised once per CTA.
+// Streaming.  Warp w of the CTA takes blocks jb + w, jb + w + 4, ... of the
+// unit's partition, in chunks of up to 16 tokens, through a private ring of
+// STAGES shared-memory stages.  One lane issues the TMA tile loads of a chunk
+// (K and V, one 128-byte-wide, 128B-swizzled slab of 64 dims per load; pool
+// layout [N, B, Hkv, D]) completing on the stage's mbarrier.  When the current
+// unit has no chunk left to load, the warp keeps loading its chunks of the
+// next unit, so the ring stays full across unit boundaries and merges.
 //
-// Per chunk: half-warp h takes half of the chunk's tokens; lane li owns
-// head_dim/16 consecutive dims.  Q.K partial dot products use the packed fp32x2
-// FMA; the (token, head) partials are summed across the 16 lanes by a
-// reduce-scatter butterfly (about one shuffle per partial instead of four).
-// Online softmax in fp32 in the exp2 domain (q pre-scaled by scale*log2 e);
-// slots at or past the context length are masked before the max and skipped
-// in P.V, so whatever bytes they hold never reach the result.  P goes to the
-// warp through shared memory as (p, p) pairs that feed the packed FMA as is.
+// Arithmetic per chunk, on the tensor cores (warp-level m16n8k16, fp32
+// accumulate), with the chunk's tokens as rows:
+//   S^T = K Q^T    A = K tile (ldmatrix), B = Q^T fragments kept in registers
+//   online softmax per query head (column), exp2 domain, fp32
+//   O^T += V^T P^T A = V tile (ldmatrix.trans), B = P^T from the S^T
+//                  fragments by an in-register 8x8 transpose (movmatrix)
+// P is fed as two 16-bit pieces (hi + lo) so that P.V keeps about 16 mantissa
+// bits; Q.K products of 16-bit inputs are exact in fp32.  The running maximum
+// used for the exponentials is raised only when a score exceeds it by more
+// than RESCALE_SLACK (exact: O and L always share the reference).  Slots at
+// or past the context length are masked before the max, and their V rows are
+// zeroed in shared memory, so whatever bytes they hold never reach the result.
 //
-// End of a unit: the warps' (max, sum, output) states merge in shared memory.
-// A one-partition sequence writes out = O / L.  Otherwise the unit writes its
-// unnormalised (M, L, O) record, bumps the sequence's completion counter, and
-// the CTA that completes the last partition merges all records:
-// o = sum_p e^(M_p - M) O_p / sum_p e^(M_p - M) L_p.  Normalising each
-// partition and adding the results would be wrong ("PagedAttention"
-// (tensortonic), section 5).  No CTA ever waits on another.
+// End of a unit: the four warps' (max, sum, O) states merge in shared memory,
+// four heads per round.  A one-partition sequence writes out = O / L.
+// Otherwise the unit writes its unnormalised (M, L, O) record and bumps the
+// sequence's completion counter; the CTA that completes the last partition
+// merges all records: o = sum_p e^(M_p - M) O_p / sum_p e^(M_p - M) L_p.
+// Normalising each partition and adding the results would be wrong
+// ("PagedAttention" (tensortonic), section 5).  No CTA ever waits on another.
 #pragma once
 
 #include <math.h>
@@ -53,54 +57,65 @@
 
 namespace pkv {
 
-constexpr int ilog2_c(int v) { return v <= 1 ? 0 : 1 + ilog2_c(v >> 1); }
 constexpr int max_c(int a, int b) { return a > b ? a : b; }
 constexpr int min_c(int a, int b) { return a < b ? a : b; }
 constexpr int round_up_c(int v, int a) { return (v + a - 1) / a * a; }
 
 constexpr int DECODE_WARPS = 4;
+constexpr int SMEM_PER_SM = 228 * 1024;   // shared memory of one SM
+constexpr int SMEM_RESERVED = 1024;       // reserved by the system per CTA
+constexpr int MERGE_HEADS = 4;            // query heads merged per round
 
-// CTAs per SM the kernel is shaped for: 3 up to 8 query heads per CTA,
-// 2 for 16 (larger merge area).
-constexpr int occupancy_for(int GT) { return GT >= 16 ? 2 : 3; }
-
-// Stages per warp: fill the shared memory of an SM across its CTAs, 2..4.
-constexpr int stages_for(int stage_bytes, int occ) {
-  return max_c(2, min_c(4, (227 * 1024 / occ - 3 * 1024) / (DECODE_WARPS * stage_bytes)));
-}
-
-// Softmax reference-max slack (log2 domain): the running maximum used for
-// the exponentials is raised only when a score exceeds it by more than this,
-// so P stays <= 2^8 and the rescale of O is rare.  Exact: O and L always use
-// the same reference.
+// Softmax reference-max slack (log2 domain): P stays <= 2^8 and the rescale
+// of O is rare.
 constexpr float RESCALE_SLACK = 8.0f;
 
-template <typename T, int D, int B, int GT>
+template <int D>
+constexpr int stage_bytes_c() { return 2 * (D / 64) * 2048; }
+template <int D>
+constexpr int merge_bytes_c() { return DECODE_WARPS * MERGE_HEADS * (D + 2) * 4; }
+template <int D>
+constexpr int smem_bytes_c(int stages) {
+  return 1024 + round_up_c(DECODE_WARPS * stages * stage_bytes_c<D>(), 1024) +
+         merge_bytes_c<D>() + DECODE_WARPS * stages * 8 + 64;
+}
+template <int D>
+constexpr bool fits_c(int stages, int occ) {
+  return (smem_bytes_c<D>(stages) + SMEM_RESERVED) * occ <= SMEM_PER_SM;
+}
+// CTAs per SM: 3 when two stages per warp fit, else 2.
+template <int D>
+constexpr int occupancy_c() { return fits_c<D>(2, 3) ? 3 : 2; }
+// Stages per warp: as many as fit (2..4).
+template <int D>
+constexpr int stages_c() {
+  return fits_c<D>(4, occupancy_c<D>()) ? 4 : (fits_c<D>(3, occupancy_c<D>()) ? 3 : 2);
+}
+
+template <typename T, int D, int B, int NH>
 struct DecodeCfg {
   static constexpr int NW = DECODE_WARPS;
-  static constexpr int OCC = occupancy_for(GT);
+  static constexpr int HEADS = 8 * NH;           // query heads per CTA (MMA N)
+  static constexpr int OCC = occupancy_c<D>();
+  static constexpr int STAGES = stages_c<D>();
   static constexpr int CH = min_c(B, 16);        // tokens per chunk (one TMA box high)
   static constexpr int NCH = B / CH;             // chunks per block
-  static constexpr int NT = (CH + 7) / 8;        // 8-token MMA n-tiles in Q.K^T
   static constexpr int NSUB = D / 64;            // 128-byte column slabs of a row
-  static constexpr int KS = D / 16;              // k-steps of Q.K^T
-  static constexpr int NTD = D / 8;              // 8-dim MMA n-tiles of P.V
+  static constexpr int KS = D / 16;              // k-steps of K Q^T
+  static constexpr int MT = D / 16;              // m-tiles (16 dims) of V^T P^T
   static constexpr int SUB_BYTES = 16 * 128;     // one slab: 16 rows x 128 B, 128B-swizzled
   static constexpr int CHUNK_BYTES = NSUB * SUB_BYTES;   // K (or V) of one chunk
   static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;    // K + V
   static constexpr int TX_BYTES = 2 * NSUB * CH * 128;   // bytes the TMA loads deliver
-  static constexpr int STAGES = stages_for(STAGE_BYTES, OCC);
-  // shared memory (bytes)
-  static constexpr int STAGES_BYTES = NW * STAGES * STAGE_BYTES;
-  static constexpr int MERGE_BYTES = NW * GT * (D + 2) * 4;
-  static constexpr int BIG_BYTES = round_up_c(max_c(STAGES_BYTES, MERGE_BYTES), 1024);
-  static constexpr int BAR_BYTES = NW * STAGES * 8;
-  static constexpr int SMEM_BYTES = 1024 + BIG_BYTES + BAR_BYTES + 16;
+  static constexpr int STAGES_BYTES = round_up_c(NW * STAGES * STAGE_BYTES, 1024);
+  static constexpr int MERGE_FLOATS = NW * MERGE_HEADS * (D + 2);
+  static constexpr int SMEM_BYTES = smem_bytes_c<D>(STAGES);
 
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(B == 4 || B == 8 || B == 16 || B == 32, "block_size");
-  static_assert(GT == 1 || GT == 4 || GT == 8 || GT == 16, "query head rows");
-  static_assert(SMEM_BYTES * OCC <= 227 * 1024, "shared memory budget");
+  static_assert(NH == 1 || NH == 2, "query head tiles");
+  static_assert(STAGE_BYTES == stage_bytes_c<D>(), "stage size");
+  static_assert(fits_c<D>(STAGES, OCC), "shared memory budget");
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
@@ -155,7 +170,8 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
     if (nb % PB) p.items[po++] = make_int2(s, F);
     if (L == 0) {   // nothing to attend to: zeros
       const size_t base = (size_t)s * p.num_q_heads * p.head_dim;
-      for (int e = 0; e < p.num_q_heads * p.head_dim; ++e) store_out(p.out, base + e, p.out_dtype, 0.f);
+      for (int e = 0; e < p.num_q_heads * p.head_dim; ++e)
+        store_out(p.out, base + e, p.out_dtype, 0.f);
     }
   }
   for (int i = tid; i < S * p.num_hc; i += 1024) p.seq_done[i] = 0u;
@@ -166,19 +182,61 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
 }
 
 // ---------------------------------------------------------------------------
-template <typename T, int D, int B, int GT>
-__global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
+// A warp's view of one work unit for loading: which blocks (and chunks) it
+// streams and its slice of the block table.
+struct WarpLoads {
+  int kvh;          // KV head
+  int j0;           // first block of this warp
+  int n_w;          // blocks of this warp
+  int n_units;      // chunks of this warp
+  int issued;       // chunks already issued
+  int kbase;        // first warp-block index held in `tbl`
+  int tbl;          // lane i: physical block of warp-block kbase + i
+  const int32_t *trow;
+};
+
+template <int B, int NCH, int CH, int NW>
+__device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodeParams &p,
+                                                  unsigned unit, int w, int lane) {
+  const int HC = p.num_hc;
+  const int2 item = __ldcg(p.items + unit / HC);
+  const int hc = (int)(unit % HC);
+  const int s = item.x, part = item.y;
+  const int L = clamp_len(__ldg(p.context_lens + s), p.max_blocks * B);
+  const int nb = (L + B - 1) / B;
+  const int jb = part * p.part_blocks;
+  const int je = min(nb, jb + p.part_blocks);
+  wl.kvh = hc / p.num_gchunks;
+  wl.j0 = jb + w;
+  wl.n_w = wl.j0 < je ? (je - wl.j0 + NW - 1) / NW : 0;
+  wl.n_units = wl.n_w * NCH;
+  if (NCH > 1 && wl.n_w > 0 && wl.j0 + (wl.n_w - 1) * NW == nb - 1) {
+    const int tail = L - (nb - 1) * B;   // tokens in the last block
+    wl.n_units -= NCH - (tail + CH - 1) / CH;
+  }
+  wl.issued = 0;
+  wl.kbase = 0;
+  wl.trow = p.block_tables + (size_t)s * p.max_blocks;
+  wl.tbl = lane < wl.n_w ? __ldg(wl.trow + wl.j0 + lane * NW) : 0;
+}
+
+// ---------------------------------------------------------------------------
+template <typename T, int D, int B, int NH>
+__global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  using C = DecodeCfg<T, D, B, GT>;
+  using C = DecodeCfg<T, D, B, NH>;
   constexpr int NW = C::NW;
   constexpr int STAGES = C::STAGES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_smem = smem_addr(smem);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BIG_BYTES);
-  volatile int *s_int = reinterpret_cast<volatile int *>(bars + NW * STAGES);  // next, abort, last
+  float *mg_o = reinterpret_cast<float *>(smem + C::STAGES_BYTES);      // [NW][4][D]
+  float *mg_ml = mg_o + NW * MERGE_HEADS * D;                          // [NW][4][2]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(mg_o + C::MERGE_FLOATS);
+  // s_int[0..2]: ring of upcoming unit ids, s_int[3]: abort, s_int[4]: last
+  volatile int *s_int = reinterpret_cast<volatile int *>(bars + NW * STAGES);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
@@ -194,8 +252,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < NW * STAGES; ++i) mbar_init(smem_addr(bars + i), 1);
-    s_int[1] = 0;
+    s_int[3] = 0;
     s_int[0] = (int)atomicAdd(p.ctrl, 1u);
+    s_int[1] = (int)atomicAdd(p.ctrl, 1u);
     fence_barrier_init();
   }
   if (tid == 32 || (NW == 1 && tid == 0)) {
@@ -211,106 +270,107 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
   uint32_t ld_cnt = 0, use_cnt = 0;   // this warp's loads issued / consumed, all units
 
   // fragment coordinates of this lane
-  const int r0 = lane >> 2;                         // C rows r0 and r0 + 8 (query heads)
-  const int cq = 2 * (lane & 3);                    // C columns cq, cq + 1
-  const int k_tok = ((lane >> 4) & 1) * 8 + (lane & 7);   // ldmatrix row for K (B operand)
-  const int k_chb = (lane >> 3) & 1;
-  const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);   // ldmatrix row for V (trans)
-  const int v_chb = (lane >> 4) & 1;
+  const int cr = lane >> 2;              // C row (token, or dim within an m-tile)
+  const int cq = 2 * (lane & 3);         // C columns (query heads) cq, cq + 1
+  const int a_tok = ((lane >> 3) & 1) * 8 + (lane & 7);   // ldmatrix row for K (A operand)
+  const int a_chb = (lane >> 4) & 1;
+  const int v_tok = ((lane >> 4) & 1) * 8 + (lane & 7);   // ldmatrix row for V (A, trans)
+  const int v_chb = (lane >> 3) & 1;
 
-  unsigned unit = (unsigned)s_int[0];
+  unsigned cur_unit = (unsigned)s_int[0];
+  unsigned nxt_unit = (unsigned)s_int[1];
+  WarpLoads cur, nxt;
+  if (cur_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(cur, p, cur_unit, w, lane);
+  if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, w, lane);
+
+  auto issue_chunk = [&](WarpLoads &wl) {
+    const int u = wl.issued++;
+    const int i = u / C::NCH;
+    const int c = u - i * C::NCH;
+    if (i - wl.kbase >= 32) {
+      wl.kbase += 32;
+      wl.tbl = wl.kbase + lane < wl.n_w ? __ldg(wl.trow + wl.j0 + (wl.kbase + lane) * NW) : 0;
+    }
+    const int pb = __shfl_sync(FULL_MASK, wl.tbl, i - wl.kbase);
+    if (lane == 0) {
+      if ((unsigned)pb >= (unsigned)p.num_blocks) atomicOr(p.flags, PKV_FLAG_BLOCK_RANGE);
+      const int stage = (int)(ld_cnt % STAGES);
+      const uint32_t bar = bar0 + stage * 8;
+      const uint32_t dst = wst + stage * C::STAGE_BYTES;
+      mbar_arrive_expect_tx(bar, C::TX_BYTES);
+      // out-of-range block ids read as zeros (TMA bounds), never fault
+#pragma unroll
+      for (int sb = 0; sb < C::NSUB; ++sb) {
+        tma_load_4d(dst + sb * C::SUB_BYTES, &kmap, sb * 64, wl.kvh, c * C::CH, pb, bar, pol);
+        tma_load_4d(dst + C::CHUNK_BYTES + sb * C::SUB_BYTES, &vmap, sb * 64, wl.kvh,
+                    c * C::CH, pb, bar, pol);
+      }
+    }
+    ++ld_cnt;
+  };
+  // Keep STAGES chunks in flight: the current unit's first, then the next's.
+  auto top_up = [&](bool have_cur, bool have_nxt) {
+    while (ld_cnt - use_cnt < (uint32_t)STAGES) {
+      if (have_cur && cur.issued < cur.n_units) issue_chunk(cur);
+      else if (have_nxt && nxt.issued < nxt.n_units) issue_chunk(nxt);
+      else break;
+    }
+  };
+  top_up(cur_unit < total, nxt_unit < total);
+
+  int qn = 2;   // ring slot the next atomicAdd result goes to
+  bool ok = true;
 #pragma unroll 1
-  while (unit < total) {
-    __syncthreads();   // every thread has read s_int[0]
-    if (tid == 0) s_int[0] = (int)atomicAdd(p.ctrl, 1u);
+  while (cur_unit < total) {
+    // the unit after `nxt_unit`; visible to all after this unit's merge barriers
+    if (tid == 0) s_int[qn] = (int)atomicAdd(p.ctrl, 1u);
 
-    const int2 item = __ldcg(p.items + unit / HC);
-    const int hc = (int)(unit % HC);
+    const int2 item = __ldcg(p.items + cur_unit / HC);
+    const int hc = (int)(cur_unit % HC);
     const int s = item.x, part = item.y;
     const int kvh = hc / p.num_gchunks;
     const int gc = hc - kvh * p.num_gchunks;
     const int L = clamp_len(__ldg(p.context_lens + s), cap);
     const int nb = (L + B - 1) / B;
-    const int jb = part * p.part_blocks;
-    const int je = min(nb, jb + p.part_blocks);
     const int nparts = (nb + p.part_blocks - 1) / p.part_blocks;
-    const int g0 = gc * GT;
-    const int gcount = min(GT, p.group - g0);
+    const int g0 = gc * C::HEADS;
+    const int gcount = min(C::HEADS, p.group - g0);
     const int hq0 = kvh * p.group + g0;
     const size_t out_base = ((size_t)s * p.num_q_heads + hq0) * D;
 
-    // ---- this warp's blocks, chunks and slice of the block table ----------
-    const int j0 = jb + w;
-    const int n_w = j0 < je ? (je - j0 + NW - 1) / NW : 0;
-    int n_units = n_w * C::NCH;
-    if (C::NCH > 1 && n_w > 0 && j0 + (n_w - 1) * NW == nb - 1) {
-      const int tail = L - (nb - 1) * B;                 // tokens in the last block
-      n_units -= C::NCH - (tail + C::CH - 1) / C::CH;
-    }
-    const int32_t *trow = p.block_tables + (size_t)s * p.max_blocks;
-    int kbase = 0;
-    int tbl = lane < n_w ? __ldg(trow + j0 + lane * NW) : 0;
-
-    auto issue = [&](int u) {
-      const int i = u / C::NCH;
-      const int c = u - i * C::NCH;
-      if (i - kbase >= 32) {
-        kbase += 32;
-        tbl = kbase + lane < n_w ? __ldg(trow + j0 + (kbase + lane) * NW) : 0;
-      }
-      const int pb = __shfl_sync(FULL_MASK, tbl, i - kbase);
-      if (lane == 0) {
-        if ((unsigned)pb >= (unsigned)p.num_blocks) atomicOr(p.flags, PKV_FLAG_BLOCK_RANGE);
-        const int stage = (int)(ld_cnt % STAGES);
-        const uint32_t bar = bar0 + stage * 8;
-        const uint32_t dst = wst + stage * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(bar, C::TX_BYTES);
-        // out-of-range block ids read as zeros (TMA bounds), never fault
-#pragma unroll
-        for (int sb = 0; sb < C::NSUB; ++sb) {
-          tma_load_4d(dst + sb * C::SUB_BYTES, &kmap, sb * 64, kvh, c * C::CH, pb, bar, pol);
-          tma_load_4d(dst + C::CHUNK_BYTES + sb * C::SUB_BYTES, &vmap, sb * 64, kvh,
-                      c * C::CH, pb, bar, pol);
-        }
-      }
-      ++ld_cnt;
-    };
-
-    // The stage area held the previous unit's merge data: every thread
-    // fenced its generic writes before the unit barrier; order them ahead of
-    // this unit's TMA writes.  Within a unit a stage is refilled only after
-    // every lane's reads of it have returned.
-    if (lane == 0) fence_proxy_async_smem();
-    int issued = 0;
-    for (; issued < n_units && issued < STAGES; ++issued) issue(issued);
-
-    // ---- query rows as MMA A fragments (rows >= gcount are zero) ----------
-    uint32_t qa[C::KS][4];
+    // ---- Q^T as B fragments (k: dims, n: heads; heads >= gcount are zero) --
+    uint32_t qb[C::KS][NH][2];
     {
-      const T *qb = static_cast<const T *>(p.q) + out_base;
+      const T *qp = static_cast<const T *>(p.q) + out_base;
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = r0 + ((e & 1) ? 8 : 0);
-          const int kk = ks * 16 + cq + ((e & 2) ? 8 : 0);
-          qa[ks][e] = row < gcount
-                          ? __ldg(reinterpret_cast<const unsigned int *>(qb + row * D + kk))
-                          : 0u;
-        }
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int head = 8 * nh + cr;
+            const int kk = ks * 16 + cq + 8 * e;
+            qb[ks][nh][e] =
+                head < gcount ? __ldg(reinterpret_cast<const unsigned int *>(qp + head * D + kk))
+                              : 0u;
+          }
     }
 
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[C::NTD][4];
+    // softmax state of heads 8nh + cq + {0, 1}
+    float mr[NH][2], lr[NH][2];
+    float o[NH][C::MT][4];
 #pragma unroll
-    for (int nt = 0; nt < C::NTD; ++nt)
+    for (int nh = 0; nh < NH; ++nh) {
+      mr[nh][0] = mr[nh][1] = -INFINITY;
+      lr[nh][0] = lr[nh][1] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nh][mt][e] = 0.f;
+    }
 
-    bool ok = true;
-    int u = 0;
 #pragma unroll 1
-    for (; u < n_units; ++u) {
+    for (int u = 0; u < cur.n_units; ++u) {
       const uint32_t stage = use_cnt % STAGES;
       const bool got = mbar_wait_bounded(bar0 + stage * 8, (use_cnt / STAGES) & 1u);
       if (!__all_sync(FULL_MASK, got)) {
@@ -319,7 +379,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
       }
       const int i = u / C::NCH;
       const int c = u - i * C::NCH;
-      const int j = j0 + i * NW;
+      const int j = cur.j0 + i * NW;
       const int valid = min(C::CH, L - j * B - c * C::CH);   // >= 1
       const uint32_t kb = wst + stage * C::STAGE_BYTES;
       const uint32_t vb = kb + C::CHUNK_BYTES;
@@ -340,199 +400,224 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_for(GT))
         __syncwarp();
       }
 
-      // S = Q K^T (rows: query heads, columns: the chunk's tokens)
-      float sa[C::NT][4];
+      // S^T = K Q^T: rows = the chunk's tokens, columns = query heads
+      float sa[NH][4];
 #pragma unroll
-      for (int jn = 0; jn < C::NT; ++jn)
+      for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sa[jn][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sa[nh][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
         const int sb = ks >> 2;
-        const int ch = (ks & 3) * 2 + k_chb;
-        const uint32_t addr = kb + sb * C::SUB_BYTES + k_tok * 128 + ((ch ^ (k_tok & 7)) << 4);
-        if (C::NT == 2) {
-          uint32_t r[4];
-          ldsm_x4(r, addr);
-          Mma<T>::run(sa[0], qa[ks], r[0], r[1]);
-          Mma<T>::run(sa[C::NT - 1], qa[ks], r[2], r[3]);
-        } else {
-          uint32_t r[2];
-          ldsm_x2(r, addr);
-          Mma<T>::run(sa[0], qa[ks], r[0], r[1]);
-        }
+        const int ch = (ks & 3) * 2 + a_chb;
+        uint32_t a[4];
+        ldsm_x4(a, kb + sb * C::SUB_BYTES + a_tok * 128 + ((ch ^ (a_tok & 7)) << 4));
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) Mma<T>::run(sa[nh], a, qb[ks][nh][0], qb[ks][nh][1]);
       }
 
-      // online softmax (exp2 domain) with a lazily raised reference max
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // online softmax per head (column), exp2 domain, lazily raised reference
+      const bool v0 = cr < valid, v1 = cr + 8 < valid;
+      bool up_any = false;
+      float mx[NH][2];
 #pragma unroll
-      for (int jn = 0; jn < C::NT; ++jn)
+      for (int nh = 0; nh < NH; ++nh) {
+        sa[nh][0] = v0 ? sa[nh][0] * p.scale_log2 : -INFINITY;
+        sa[nh][1] = v0 ? sa[nh][1] * p.scale_log2 : -INFINITY;
+        sa[nh][2] = v1 ? sa[nh][2] * p.scale_log2 : -INFINITY;
+        sa[nh][3] = v1 ? sa[nh][3] * p.scale_log2 : -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = 8 * jn + cq + (e & 1);
-          const float x = tok < valid ? sa[jn][e] * p.scale_log2 : -INFINITY;
-          sa[jn][e] = x;
-          if (e < 2) mx0 = fmaxf(mx0, x); else mx1 = fmaxf(mx1, x);
-        }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
-      const bool up0 = mx0 > m0 + RESCALE_SLACK, up1 = mx1 > m1 + RESCALE_SLACK;
-      if (__any_sync(FULL_MASK, up0 || up1)) {
-        const float n0 = up0 ? mx0 : m0, n1 = up1 ? mx1 : m1;
-        const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        l0 *= a0;
-        l1 *= a1;
-#pragma unroll
-        for (int nt = 0; nt < C::NTD; ++nt) {
-          o[nt][0] *= a0; o[nt][1] *= a0;
-          o[nt][2] *= a1; o[nt][3] *= a1;
+        for (int hh = 0; hh < 2; ++hh) {
+          float x = fmaxf(sa[nh][hh], sa[nh][hh + 2]);
+          x = fmaxf(x, __shfl_xor_sync(FULL_MASK, x, 4));
+          x = fmaxf(x, __shfl_xor_sync(FULL_MASK, x, 8));
+          x = fmaxf(x, __shfl_xor_sync(FULL_MASK, x, 16));
+          mx[nh][hh] = x;
+          up_any |= x > mr[nh][hh] + RESCALE_SLACK;
         }
       }
-      uint32_t ah[4], al[4];
+      if (__any_sync(FULL_MASK, up_any)) {
 #pragma unroll
-      for (int jn = 0; jn < 2; ++jn) {
-        if (jn < C::NT) {
-          const float p00 = fast_exp2(sa[jn][0] - m0), p01 = fast_exp2(sa[jn][1] - m0);
-          const float p10 = fast_exp2(sa[jn][2] - m1), p11 = fast_exp2(sa[jn][3] - m1);
-          l0 += p00 + p01;
-          l1 += p10 + p11;
-          // P in two 16-bit pieces (hi + lo) keeps about 16 mantissa bits
-          const uint32_t h0 = Mma<T>::pack(p00, p01), h1 = Mma<T>::pack(p10, p11);
-          const float2 b0 = Widen<T>::pair(h0), b1 = Widen<T>::pair(h1);
-          ah[2 * jn + 0] = h0;
-          ah[2 * jn + 1] = h1;
-          al[2 * jn + 0] = Mma<T>::pack(p00 - b0.x, p01 - b0.y);
-          al[2 * jn + 1] = Mma<T>::pack(p10 - b1.x, p11 - b1.y);
-        } else {
-          ah[2 * jn] = ah[2 * jn + 1] = al[2 * jn] = al[2 * jn + 1] = 0u;
+        for (int nh = 0; nh < NH; ++nh) {
+          float a2[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float nm = mx[nh][hh] > mr[nh][hh] + RESCALE_SLACK ? mx[nh][hh] : mr[nh][hh];
+            a2[hh] = fast_exp2(mr[nh][hh] - nm);
+            mr[nh][hh] = nm;
+            lr[nh][hh] *= a2[hh];
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            o[nh][mt][0] *= a2[0];
+            o[nh][mt][1] *= a2[1];
+            o[nh][mt][2] *= a2[0];
+            o[nh][mt][3] *= a2[1];
+          }
         }
+      }
+      uint32_t bh[NH][2], bl[NH][2];
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) {
+        const float p0 = fast_exp2(sa[nh][0] - mr[nh][0]), p1 = fast_exp2(sa[nh][1] - mr[nh][1]);
+        const float p2 = fast_exp2(sa[nh][2] - mr[nh][0]), p3 = fast_exp2(sa[nh][3] - mr[nh][1]);
+        lr[nh][0] += p0 + p2;
+        lr[nh][1] += p1 + p3;
+        // P^T rows (tokens) as 16-bit pairs, hi and lo pieces, transposed into
+        // B fragments (k: tokens, n: heads)
+        const uint32_t ht = Mma<T>::pack(p0, p1), hb = Mma<T>::pack(p2, p3);
+        const float2 ft = Widen<T>::pair(ht), fb = Widen<T>::pair(hb);
+        const uint32_t lt = Mma<T>::pack(p0 - ft.x, p1 - ft.y);
+        const uint32_t lb = Mma<T>::pack(p2 - fb.x, p3 - fb.y);
+        bh[nh][0] = movmatrix_trans(ht);
+        bh[nh][1] = movmatrix_trans(hb);
+        bl[nh][0] = movmatrix_trans(lt);
+        bl[nh][1] = movmatrix_trans(lb);
       }
 
-      // O += P V
+      // O^T += V^T P^T: rows = dims (m-tiles of 16), columns = query heads
 #pragma unroll
-      for (int nt = 0; nt < C::NTD; nt += 2) {
-        const int sb = nt >> 3;
-        const int ch = (nt & 7) + v_chb;
-        uint32_t r[4];
-        ldsm_x4_trans(r, vb + sb * C::SUB_BYTES + v_tok * 128 + ((ch ^ (v_tok & 7)) << 4));
-        Mma<T>::run(o[nt], ah, r[0], r[1]);
-        Mma<T>::run(o[nt], al, r[0], r[1]);
-        Mma<T>::run(o[nt + 1], ah, r[2], r[3]);
-        Mma<T>::run(o[nt + 1], al, r[2], r[3]);
+      for (int mt = 0; mt < C::MT; ++mt) {
+        const int sb = mt >> 2;
+        const int ch = (mt & 3) * 2 + v_chb;
+        uint32_t a[4];
+        ldsm_x4_trans(a, vb + sb * C::SUB_BYTES + v_tok * 128 + ((ch ^ (v_tok & 7)) << 4));
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) {
+          Mma<T>::run(o[nh][mt], a, bh[nh][0], bh[nh][1]);
+          Mma<T>::run(o[nh][mt], a, bl[nh][0], bl[nh][1]);
+        }
       }
       __syncwarp();   // every lane's reads of this stage have returned
       ++use_cnt;
-      if (issued < n_units) {
-        issue(issued);
-        ++issued;
-      }
+      top_up(true, nxt_unit < total);
     }
 
-    if (!ok) {
-      if (lane == 0) {
-        atomicOr(p.flags, PKV_FLAG_TIMEOUT);
-        s_int[1] = 1;
-      }
-      // let this warp's copies land before the stages are reused or released
-      for (; use_cnt < ld_cnt; ++use_cnt)
-        (void)mbar_wait_bounded(bar0 + (use_cnt % STAGES) * 8, (use_cnt / STAGES) & 1u);
+    if (!ok && lane == 0) {
+      atomicOr(p.flags, PKV_FLAG_TIMEOUT);
+      s_int[3] = 1;
     }
 
-    // row sums: the 4 lanes of a row hold different columns
-    l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
-    l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
-    l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
-    l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
-
-    __syncthreads();  // every stage consumed: the stage area becomes merge space
-    float *mg_o = reinterpret_cast<float *>(smem);    // [NW][GT][D]
-    float *mg_ml = mg_o + NW * GT * D;                 // [NW][GT][2]
+    // ---- merge the four warps' states, MERGE_HEADS heads per round --------
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int row = r0 + 8 * hr;
-      if (row < gcount) {
+    for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int nt = 0; nt < C::NTD; ++nt)
-          *reinterpret_cast<float2 *>(mg_o + (w * GT + row) * D + 8 * nt + cq) =
-              make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
-        if ((lane & 3) == 0) {
-          mg_ml[(w * GT + row) * 2 + 0] = hr ? m1 : m0;
-          mg_ml[(w * GT + row) * 2 + 1] = hr ? l1 : l0;
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        float x = lr[nh][hh];
+        x += __shfl_xor_sync(FULL_MASK, x, 4);
+        x += __shfl_xor_sync(FULL_MASK, x, 8);
+        x += __shfl_xor_sync(FULL_MASK, x, 16);
+        lr[nh][hh] = x;
       }
-    }
-    __syncthreads();
-    const bool abort = s_int[1] != 0;
-    if (!abort) {
-      for (int idx = tid; idx < gcount * D; idx += NW * 32) {
-        const int g = idx / D;
-        const int d = idx - g * D;
-        float M = -INFINITY;
+    for (int h0 = 0; h0 < gcount; h0 += MERGE_HEADS) {
+      const int hn = min(MERGE_HEADS, gcount - h0);
 #pragma unroll
-        for (int x = 0; x < NW; ++x) M = fmaxf(M, mg_ml[(x * GT + g) * 2]);
-        float Lt = 0.f, O = 0.f;
+      for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int x = 0; x < NW; ++x) {
-          const float f = fast_exp2(mg_ml[(x * GT + g) * 2] - M);
-          Lt += f * mg_ml[(x * GT + g) * 2 + 1];
-          O += f * mg_o[(x * GT + g) * D + d];
-        }
-        if (nparts == 1) {
-          store_out(p.out, out_base + idx, p.out_dtype, O / Lt);
-        } else {
-          const size_t rec = ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts + part;
-          p.part_o[rec * D + d] = O;
-          if (d == 0) {
-            p.part_ml[rec * 2 + 0] = M;
-            p.part_ml[rec * 2 + 1] = Lt;
-          }
-        }
-      }
-      if (nparts > 1) {
-        // Release this CTA's records (ordered before thread 0 by the barrier)
-        // with one gpu-scope fence before the counter update; the CTA that
-        // sees the final count fences again before reading the others'.
-        __syncthreads();
-        if (tid == 0) {
-          __threadfence();
-          const unsigned prev = atomicAdd(p.seq_done + (size_t)s * HC + hc, 1u);
-          const bool last = prev == (unsigned)(nparts - 1);
-          if (last) __threadfence();
-          s_int[2] = last;
-        }
-        __syncthreads();
-        if (s_int[2]) {   // this CTA completed the sequence's last partition
-          for (int idx = tid; idx < gcount * D; idx += NW * 32) {
-            const int g = idx / D;
-            const int d = idx - g * D;
-            const size_t rec0 = ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts;
-            float M = -INFINITY;
-            for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(p.part_ml + (rec0 + q) * 2));
-            float Lt = 0.f, O = 0.f;
-            for (int q = 0; q < nparts; ++q) {
-              const float f = fast_exp2(__ldcg(p.part_ml + (rec0 + q) * 2) - M);
-              Lt += f * __ldcg(p.part_ml + (rec0 + q) * 2 + 1);
-              O += f * __ldcg(p.part_o + (rec0 + q) * D + d);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int head = 8 * nh + cq + hh;
+          if (head >= h0 && head < h0 + hn) {
+            const int slot = w * MERGE_HEADS + (head - h0);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+              mg_o[slot * D + 16 * mt + cr] = o[nh][mt][hh];
+              mg_o[slot * D + 16 * mt + cr + 8] = o[nh][mt][hh + 2];
             }
-            store_out(p.out, out_base + idx, p.out_dtype, O / Lt);
+            if (cr == 0) {
+              mg_ml[slot * 2 + 0] = mr[nh][hh];
+              mg_ml[slot * 2 + 1] = lr[nh][hh];
+            }
+          }
+        }
+      __syncthreads();
+      if (s_int[3] == 0) {
+        for (int idx = tid; idx < hn * D; idx += NW * 32) {
+          const int g = idx / D;
+          const int d = idx - g * D;
+          float M = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < NW; ++x) M = fmaxf(M, mg_ml[(x * MERGE_HEADS + g) * 2]);
+          float Lt = 0.f, O = 0.f;
+#pragma unroll
+          for (int x = 0; x < NW; ++x) {
+            const float f = fast_exp2(mg_ml[(x * MERGE_HEADS + g) * 2] - M);
+            Lt += f * mg_ml[(x * MERGE_HEADS + g) * 2 + 1];
+            O += f * mg_o[(x * MERGE_HEADS + g) * D + d];
+          }
+          const int head = h0 + g;
+          if (nparts == 1) {
+            store_out(p.out, out_base + (size_t)head * D + d, p.out_dtype, O / Lt);
+          } else {
+            const size_t rec = ((size_t)s * p.num_q_heads + hq0 + head) * p.max_parts + part;
+            p.part_o[rec * D + d] = O;
+            if (d == 0) {
+              p.part_ml[rec * 2 + 0] = M;
+              p.part_ml[rec * 2 + 1] = Lt;
+            }
           }
         }
       }
+      __syncthreads();   // merge slots free again; this round's records written
     }
-    __syncthreads();  // merge reads done
-    if (C::CH < 16) {   // the merge overwrote rows that must stay zero
-      for (int i2 = tid; i2 < C::MERGE_BYTES / 16; i2 += NW * 32)
-        *reinterpret_cast<uint4 *>(smem + i2 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    const bool abort = s_int[3] != 0;
+
+    // ---- split-context completion: the CTA that wrote a sequence's last
+    // partition record merges all of them (one pass, running max) ----------
+    if (!abort && nparts > 1) {
+      if (tid == 0) {
+        __threadfence();   // release the records (ordered before by the barrier)
+        const bool last =
+            atomicAdd(p.seq_done + (size_t)s * HC + hc, 1u) == (unsigned)(nparts - 1);
+        if (last) __threadfence();
+        s_int[4] = last;
+      }
+      __syncthreads();
+      if (s_int[4]) {
+        constexpr int Q4 = D / 4;   // threads per head, 4 dims each
+        for (int idx = tid; idx < gcount * Q4; idx += NW * 32) {
+          const int g = idx / Q4;
+          const int d4 = idx - g * Q4;
+          const size_t rec0 = ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts;
+          float M = -INFINITY, Lt = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int q = 0; q < nparts; ++q) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + rec0 + q);
+            const float4 ov =
+                __ldcg(reinterpret_cast<const float4 *>(p.part_o + (rec0 + q) * D) + d4);
+            const float Mn = fmaxf(M, ml.x);
+            const float a = fast_exp2(M - Mn), f = fast_exp2(ml.x - Mn);
+            acc.x = acc.x * a + f * ov.x;
+            acc.y = acc.y * a + f * ov.y;
+            acc.z = acc.z * a + f * ov.z;
+            acc.w = acc.w * a + f * ov.w;
+            Lt = Lt * a + f * ml.y;
+            M = Mn;
+          }
+          const float inv = 1.f / Lt;
+          const size_t ob = out_base + (size_t)g * D + 4 * d4;
+          store_out(p.out, ob + 0, p.out_dtype, acc.x * inv);
+          store_out(p.out, ob + 1, p.out_dtype, acc.y * inv);
+          store_out(p.out, ob + 2, p.out_dtype, acc.z * inv);
+          store_out(p.out, ob + 3, p.out_dtype, acc.w * inv);
+        }
+      }
     }
-    fence_proxy_async_smem();
-    __syncthreads();  // stage area free again; s_int[0] holds the next unit
     if (abort) break;
-    unit = (unsigned)s_int[0];
+
+    // ---- advance: the next unit becomes current (its first chunks may be
+    // in flight already); learn the one after it from the ring -------------
+    cur_unit = nxt_unit;
+    cur = nxt;
+    nxt_unit = (unsigned)s_int[qn];
+    qn = qn == 2 ? 0 : qn + 1;
+    if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, w, lane);
+    top_up(cur_unit < total, nxt_unit < total);
   }
+
+  // never leave with copies in flight into this CTA's shared memory
+  for (; use_cnt < ld_cnt; ++use_cnt)
+    (void)mbar_wait_bounded(bar0 + (use_cnt % STAGES) * 8, (use_cnt / STAGES) & 1u);
 }
 
 // ---- host-side launch -------------------------------------------------------
@@ -573,11 +658,11 @@ cudaError_t launch_info(const void *fn, int threads, int smem, int dev, LaunchIn
 }
 }  // namespace
 
-template <typename T, int D, int B, int GT>
+template <typename T, int D, int B, int NH>
 cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeParams &p, cudaStream_t stream, int *launches) {
-  using C = DecodeCfg<T, D, B, GT>;
-  auto kern = decode_kernel<T, D, B, GT>;
+  using C = DecodeCfg<T, D, B, NH>;
+  auto kern = decode_kernel<T, D, B, NH>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -601,13 +686,10 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
 }
 
 template <typename T, int D, int B>
-cudaError_t launch_decode_gt(const CUtensorMap &kmap, const CUtensorMap &vmap,
+cudaError_t launch_decode_nh(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, cudaStream_t stream, int *launches) {
-  const int g = p.group >= 16 ? 16 : p.group;
-  if (g <= 1) return launch_decode_cfg<T, D, B, 1>(kmap, vmap, p, stream, launches);
-  if (g <= 4) return launch_decode_cfg<T, D, B, 4>(kmap, vmap, p, stream, launches);
-  if (g <= 8) return launch_decode_cfg<T, D, B, 8>(kmap, vmap, p, stream, launches);
-  return launch_decode_cfg<T, D, B, 16>(kmap, vmap, p, stream, launches);
+  if (p.group <= 8) return launch_decode_cfg<T, D, B, 1>(kmap, vmap, p, stream, launches);
+  return launch_decode_cfg<T, D, B, 2>(kmap, vmap, p, stream, launches);
 }
 
 template <typename T, int D>
@@ -615,10 +697,10 @@ cudaError_t launch_decode_b(const CUtensorMap &kmap, const CUtensorMap &vmap,
                             const DecodeParams &p, int block_size, cudaStream_t stream,
                             int *launches) {
   switch (block_size) {
-    case 4: return launch_decode_gt<T, D, 4>(kmap, vmap, p, stream, launches);
-    case 8: return launch_decode_gt<T, D, 8>(kmap, vmap, p, stream, launches);
-    case 16: return launch_decode_gt<T, D, 16>(kmap, vmap, p, stream, launches);
-    case 32: return launch_decode_gt<T, D, 32>(kmap, vmap, p, stream, launches);
+    case 4: return launch_decode_nh<T, D, 4>(kmap, vmap, p, stream, launches);
+    case 8: return launch_decode_nh<T, D, 8>(kmap, vmap, p, stream, launches);
+    case 16: return launch_decode_nh<T, D, 16>(kmap, vmap, p, stream, launches);
+    case 32: return launch_decode_nh<T, D, 32>(kmap, vmap, p, stream, launches);
     default: return cudaErrorInvalidValue;
   }
 }
