@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(COPY_THREADS)
     block_copy_kernel(uint4 *k_cache, uint4 *v_cache, const int64_t *__restrict__ pairs,
                       int num_pairs, long long block_vecs, int chunks, int num_blocks,
                       unsigned *flags) {
+  pdl_launch_dependents();
+  pdl_wait_predecessors();   // the pool may be written or read by earlier kernels
   const int pair = blockIdx.x / chunks;
   const int chunk = blockIdx.x - pair * chunks;
   if (pair >= num_pairs) return;
@@ -50,11 +52,9 @@ cudaError_t launch_block_copy(void *k_cache, void *v_cache, const int64_t *pairs
   const int chunks = (int)((block_vecs + COPY_CHUNK_VECS - 1) / COPY_CHUNK_VECS);
   const long long gx = (long long)num_pairs * chunks;
   if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)gx, 2);
-  block_copy_kernel<<<grid, COPY_THREADS, 0, stream>>>(
-      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, num_pairs,
-      block_vecs, chunks, num_blocks, flags);
-  return cudaGetLastError();
+  return launch_pdl(block_copy_kernel, dim3((unsigned)gx, 2), dim3(COPY_THREADS), 0, stream,
+                    static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs,
+                    num_pairs, block_vecs, chunks, num_blocks, flags);
 }
 
 }  // namespace pkv

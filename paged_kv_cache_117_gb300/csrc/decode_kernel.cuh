@@ -83,21 +83,22 @@ template <int D>
 constexpr bool fits_c(int stages, int occ) {
   return (smem_bytes_c<D>(stages) + SMEM_RESERVED) * occ <= SMEM_PER_SM;
 }
-// CTAs per SM: 3 when two stages per warp fit, else 2.
-template <int D>
-constexpr int occupancy_c() { return fits_c<D>(2, 3) ? 3 : 2; }
+// CTAs per SM: 3 when two stages per warp fit and the registers allow it
+// (one 8-head tile), else 2.
+template <int D, int NH>
+constexpr int occupancy_c() { return (NH == 1 && fits_c<D>(2, 3)) ? 3 : 2; }
 // Stages per warp: as many as fit (2..4).
-template <int D>
+template <int D, int NH>
 constexpr int stages_c() {
-  return fits_c<D>(4, occupancy_c<D>()) ? 4 : (fits_c<D>(3, occupancy_c<D>()) ? 3 : 2);
+  return fits_c<D>(4, occupancy_c<D, NH>()) ? 4 : (fits_c<D>(3, occupancy_c<D, NH>()) ? 3 : 2);
 }
 
 template <typename T, int D, int B, int NH>
 struct DecodeCfg {
   static constexpr int NW = DECODE_WARPS;
   static constexpr int HEADS = 8 * NH;           // query heads per CTA (MMA N)
-  static constexpr int OCC = occupancy_c<D>();
-  static constexpr int STAGES = stages_c<D>();
+  static constexpr int OCC = occupancy_c<D, NH>();
+  static constexpr int STAGES = stages_c<D, NH>();
   static constexpr int CH = min_c(B, 16);        // tokens per chunk (one TMA box high)
   static constexpr int NCH = B / CH;             // chunks per block
   static constexpr int NSUB = D / 64;            // 128-byte column slabs of a row
@@ -124,6 +125,8 @@ __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L
 // Work list: one CTA of 1024 threads.
 static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
   __shared__ int wsum_f[32], wsum_p[32];
+  pdl_launch_dependents();   // the attention grid may start its prologue
+  pdl_wait_predecessors();   // context_lens / out may come from earlier kernels
   const int S = p.num_seqs, PB = p.part_blocks, Bs = p.block_size;
   const int cap = p.max_blocks * Bs;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -185,6 +188,10 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
 // A warp's view of one work unit for loading: which blocks (and chunks) it
 // streams and its slice of the block table.
 struct WarpLoads {
+  int s;            // sequence
+  int part;         // partition
+  int hc;           // KV head x query-head chunk index
+  int L;            // context length (clamped)
   int kvh;          // KV head
   int j0;           // first block of this warp
   int n_w;          // blocks of this warp
@@ -206,6 +213,10 @@ __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodePar
   const int nb = (L + B - 1) / B;
   const int jb = part * p.part_blocks;
   const int je = min(nb, jb + p.part_blocks);
+  wl.s = s;
+  wl.part = part;
+  wl.hc = hc;
+  wl.L = L;
   wl.kvh = hc / p.num_gchunks;
   wl.j0 = jb + w;
   wl.n_w = wl.j0 < je ? (je - wl.j0 + NW - 1) / NW : 0;
@@ -220,9 +231,32 @@ __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodePar
   wl.tbl = lane < wl.n_w ? __ldg(wl.trow + wl.j0 + lane * NW) : 0;
 }
 
+// Q^T of one unit as MMA B fragments (k: dims, n: heads); heads past the
+// group are zero.
+template <typename T, int D, int NH, int HEADS>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qb)[D / 16][NH][2], const DecodeParams &p,
+                                             const WarpLoads &wl, int cr, int cq) {
+  const int gc = wl.hc - wl.kvh * p.num_gchunks;
+  const int g0 = gc * HEADS;
+  const int gcount = min(HEADS, p.group - g0);
+  const T *qp = static_cast<const T *>(p.q) +
+                ((size_t)wl.s * p.num_q_heads + wl.kvh * p.group + g0) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int head = 8 * nh + cr;
+        const int kk = ks * 16 + cq + 8 * e;
+        qb[ks][nh][e] =
+            head < gcount ? __ldg(reinterpret_cast<const unsigned int *>(qp + head * D + kk)) : 0u;
+      }
+}
+
 // ---------------------------------------------------------------------------
 template <typename T, int D, int B, int NH>
-__global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
+__global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using C = DecodeCfg<T, D, B, NH>;
@@ -241,7 +275,6 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
   const int HC = p.num_hc;
-  const int cap = p.max_blocks * B;
 
   // Rows a chunk never loads (block_size < 16) must read as zeros in P.V.
   if (C::CH < 16) {
@@ -253,13 +286,18 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
 #pragma unroll 1
     for (int i = 0; i < NW * STAGES; ++i) mbar_init(smem_addr(bars + i), 1);
     s_int[3] = 0;
-    s_int[0] = (int)atomicAdd(p.ctrl, 1u);
-    s_int[1] = (int)atomicAdd(p.ctrl, 1u);
     fence_barrier_init();
   }
   if (tid == 32 || (NW == 1 && tid == 0)) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+  }
+  // everything above is local; the work list, the pool and q come from the
+  // kernels before this one
+  pdl_wait_predecessors();
+  if (tid == 0) {
+    s_int[0] = (int)atomicAdd(p.ctrl, 1u);
+    s_int[1] = (int)atomicAdd(p.ctrl, 1u);
   }
   const unsigned total = __ldcg(p.ctrl + 1);
   __syncthreads();
@@ -318,6 +356,11 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
   };
   top_up(cur_unit < total, nxt_unit < total);
 
+  // query fragments of the current unit; the next unit's are loaded one unit
+  // ahead so that a unit starts without waiting for them
+  uint32_t qb[C::KS][NH][2], qb_next[C::KS][NH][2];
+  if (cur_unit < total) load_q_frags<T, D, NH, C::HEADS>(qb, p, cur, cr, cq);
+
   int qn = 2;   // ring slot the next atomicAdd result goes to
   bool ok = true;
 #pragma unroll 1
@@ -325,36 +368,16 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
     // the unit after `nxt_unit`; visible to all after this unit's merge barriers
     if (tid == 0) s_int[qn] = (int)atomicAdd(p.ctrl, 1u);
 
-    const int2 item = __ldcg(p.items + cur_unit / HC);
-    const int hc = (int)(cur_unit % HC);
-    const int s = item.x, part = item.y;
-    const int kvh = hc / p.num_gchunks;
+    if (nxt_unit < total) load_q_frags<T, D, NH, C::HEADS>(qb_next, p, nxt, cr, cq);
+    const int s = cur.s, part = cur.part, hc = cur.hc, L = cur.L;
+    const int kvh = cur.kvh;
     const int gc = hc - kvh * p.num_gchunks;
-    const int L = clamp_len(__ldg(p.context_lens + s), cap);
     const int nb = (L + B - 1) / B;
     const int nparts = (nb + p.part_blocks - 1) / p.part_blocks;
     const int g0 = gc * C::HEADS;
     const int gcount = min(C::HEADS, p.group - g0);
     const int hq0 = kvh * p.group + g0;
     const size_t out_base = ((size_t)s * p.num_q_heads + hq0) * D;
-
-    // ---- Q^T as B fragments (k: dims, n: heads; heads >= gcount are zero) --
-    uint32_t qb[C::KS][NH][2];
-    {
-      const T *qp = static_cast<const T *>(p.q) + out_base;
-#pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks)
-#pragma unroll
-        for (int nh = 0; nh < NH; ++nh)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int head = 8 * nh + cr;
-            const int kk = ks * 16 + cq + 8 * e;
-            qb[ks][nh][e] =
-                head < gcount ? __ldg(reinterpret_cast<const unsigned int *>(qp + head * D + kk))
-                              : 0u;
-          }
-    }
 
     // softmax state of heads 8nh + cq + {0, 1}
     float mr[NH][2], lr[NH][2];
@@ -609,6 +632,13 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
     // in flight already); learn the one after it from the ring -------------
     cur_unit = nxt_unit;
     cur = nxt;
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) {
+        qb[ks][nh][0] = qb_next[ks][nh][0];
+        qb[ks][nh][1] = qb_next[ks][nh][1];
+      }
     nxt_unit = (unsigned)s_int[qn];
     qn = qn == 2 ? 0 : qn + 1;
     if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, w, lane);
@@ -618,6 +648,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D>())
   // never leave with copies in flight into this CTA's shared memory
   for (; use_cnt < ld_cnt; ++use_cnt)
     (void)mbar_wait_bounded(bar0 + (use_cnt % STAGES) * 8, (use_cnt / STAGES) & 1u);
+  pdl_launch_dependents();
 }
 
 // ---- host-side launch -------------------------------------------------------
@@ -669,8 +700,7 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
   LaunchInfo li;
   e = launch_info(reinterpret_cast<const void *>(kern), C::NW * 32, C::SMEM_BYTES, dev, &li);
   if (e != cudaSuccess) return e;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, p);
   if (e != cudaSuccess) return e;
   ++*launches;
   const long long units_max =
@@ -678,8 +708,8 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
   long long grid = (long long)li.sms * li.ctas_per_sm;
   if (grid > units_max) grid = units_max;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, C::NW * 32, C::SMEM_BYTES, stream>>>(kmap, vmap, p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::NW * 32), C::SMEM_BYTES, stream, kmap, vmap,
+                 p);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaSuccess;

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256)
                     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                     const int64_t *__restrict__ slots, int num_tokens, int row_vecs,
                     long long num_slots, unsigned *flags) {
+  pdl_launch_dependents();
+  pdl_wait_predecessors();   // inputs may come from, and the pool be read by, earlier kernels
   const long long total = (long long)num_tokens * row_vecs;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -43,11 +45,10 @@ cudaError_t launch_kv_write(const void *key, const void *value, void *k_cache,
   const long long total = (long long)num_tokens * row_vecs;
   long long blocks = (total + 255) / 256;
   if (blocks > 152LL * 32) blocks = 152LL * 32;
-  kv_write_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slots, num_tokens,
-      row_vecs, num_slots, flags);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                    static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                    static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slots,
+                    num_tokens, row_vecs, num_slots, flags);
 }
 
 }  // namespace pkv

@@ -90,6 +90,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Kernels of this library are launched with programmatic stream
+// serialization: each lets its successor start launching early, and waits
+// for its predecessors to finish (and their writes to be visible) before it
+// touches memory they may produce or consume.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_predecessors() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- 16-bit -> fp32 --------------------------------------------------------
 // A 32-bit word holds two consecutive 16-bit elements, element 0 in the low
 // half.  bf16 is the top half of an fp32, so widening is a shift or a mask.

@@ -77,6 +77,25 @@ cudaError_t launch_decode_f16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeParams &p, int head_dim, int block_size,
                               cudaStream_t stream, int *launches);
 
+// Launches `kern` with programmatic stream serialization allowed, so that
+// its launch overlaps the tail of the previous kernel on `stream`.  The
+// kernels call griddepcontrol.wait before touching shared data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_kv_write(const void *key, const void *value, void *k_cache,
                             void *v_cache, const int64_t *slots, int num_tokens,
                             int row_bytes, long long num_slots, unsigned *flags,

@@ -68,7 +68,7 @@ TINY = Workload("tiny", 4, 4, 4, 64, 4, 64, torch.bfloat16, 0, 118,
                 "fixed", (1, 6, 9, 17))
 OPT13B = Workload("opt13b", 64, 40, 40, 128, 16, 10_000, torch.float16, 512, 119,
                   "uniform", (128, 2048))
-LLAMA8B = Workload("llama8b", 256, 32, 8, 128, 16, 40_000, torch.bfloat16, 512, 120,
+LLAMA8B = Workload("llama8b", 256, 32, 8, 128, 16, 40_000, torch.bfloat16, 768, 120,
                    "lognormal", (1024.0, 0.8, 16, 8192))
 QWEN72B = Workload("qwen72b", 32, 64, 8, 128, 16, 20_480, torch.bfloat16, 512, 121,
                    "fixed", (8192,) * 32)
