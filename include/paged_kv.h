@@ -181,6 +181,41 @@ size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
                                        int head_dim, int max_context,
                                        int partition_tokens);
 
+/*
+ * paged_attention_decode_noalloc -- paged_attention_decode without a
+ * caller-provided workspace.  (The pages describe no such call: it exists for
+ * callers of this library that cannot allocate device memory.)
+ *
+ * Some callers cannot hand the library a scratch buffer: a host program
+ * whose device memory belongs to another memory manager that gives out no
+ * extra buffers, a plugin inside a host process with a fixed memory budget
+ * reserved up front, or a latency-critical loop that must not call cudaMalloc
+ * (it can synchronise the device).  This entry point computes exactly what
+ * paged_attention_decode computes, with the same arguments minus `workspace`
+ * and `workspace_bytes`; its scratch is a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES that is part of the library's device image, held
+ * on every GPU that loads the library until the process exits.  Nothing is
+ * allocated by the call.
+ *
+ *  - Limit: a request whose paged_attention_workspace_bytes(num_seqs,
+ *    num_q_heads, head_dim, max_blocks * block_size, partition_tokens)
+ *    exceeds PKV_NOALLOC_SCRATCH_BYTES returns PKV_ERR_WORKSPACE before any
+ *    CUDA call.
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address once; make that first call before any stream
+ *    capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    last call's contents (the call resets what must start at zero).  Calls
+ *    that overlap in time on one device race; order them on one stream.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (64u << 20)
+pkv_status paged_attention_decode_noalloc(
+    void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
+    const void *v_cache, pkv_dtype dtype, const int32_t *block_tables,
+    int max_blocks, const int32_t *context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, float scale, int partition_tokens, pkv_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *pkv_status_string(pkv_status status);
 

@@ -33,7 +33,11 @@ EXPORTED_SYMBOLS = (
     "pkv_status_string",
     "pkv_read_device_flags",
     "pkv_last_error_string",
+    "paged_attention_decode_noalloc",
 )
+
+# Fixed scratch size of paged_attention_decode_noalloc (PKV_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class PkvError(RuntimeError):
@@ -73,6 +77,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_read_device_flags.restype = ci
     lib.pkv_last_error_string.argtypes = []
     lib.pkv_last_error_string.restype = ctypes.c_char_p
+    lib.paged_attention_decode_noalloc.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, ci, ci,
+                                                   ci, ci, ci, ci, cf, ci, vp]
+    lib.paged_attention_decode_noalloc.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -164,6 +171,27 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         S, Hq, Hkv, D, B, N, float(scale), int(partition_tokens), _ptr(workspace), ws_bytes,
         _stream(stream))
     _check("paged_attention_decode", st)
+    return out
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   scale, partition_tokens=512, stream=None):
+    """paged_attention_decode for callers that cannot allocate a workspace:
+    the library's own fixed scratch (NOALLOC_SCRATCH_BYTES per device) is
+    used instead.  Calls that overlap in time on one device must not be
+    issued (they share that scratch)."""
+    _need_cuda("paged_attention_decode_noalloc", out, q, k_cache, v_cache, block_tables,
+               context_lens)
+    N, B, Hkv, D = _cache_dims(k_cache)
+    S, Hq, _ = (int(x) for x in q.shape)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    st = load().paged_attention_decode_noalloc(
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(context_lens), S, Hq, Hkv, D, B, N, float(scale), int(partition_tokens),
+        _stream(stream))
+    _check("paged_attention_decode_noalloc", st)
     return out
 
 
