@@ -92,6 +92,32 @@ def peak_hbm():
         return 6800.0, "fallback"
 
 
+DECODE_SOURCES = ("paged_kv_cache_117_gb300/csrc/decode_kernel.cuh",
+                  "paged_kv_cache_117_gb300/csrc/pkv_device.cuh",
+                  "paged_kv_cache_117_gb300/csrc/pkv_launch.h",
+                  "paged_kv_cache_117_gb300/csrc/capi.cu")
+
+
+def measured_traffic(workload, partition_tokens):
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    when it was taken on another workload or the decode sources changed since."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", "decode_kernel_llama8b.md")).read()
+        kv = dict(line.split(": ", 1) for line in text.splitlines()
+                  if line.startswith(("traffic_", "source_sha256")))
+        h = hashlib.sha256()
+        for f in DECODE_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        if (kv.get("source_sha256") == h.hexdigest() and kv.get("traffic_workload") == workload
+                and int(kv.get("traffic_partition_tokens", -1)) == partition_tokens):
+            return int(kv["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def workload_desc(w, width):
     lk = {"lognormal": "lognormal lengths (median %g, sigma %g, clipped to [%d, %d])",
           "uniform": "uniform lengths in [%d, %d]", "fixed": "fixed lengths"}[w.lens_kind]
@@ -357,7 +383,8 @@ def run_native(a, world, rank, local):
         "roofline": {"kernel": "paged_attention_decode (work list + attention with fused merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4),
+                     "traffic": measured_traffic(w.name, pt)},
         "e2e": {"value": round(world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
