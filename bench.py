@@ -34,7 +34,8 @@ from paged_kv_cache_117_gb300 import workloads as wl  # noqa: E402
 METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 UNIT = "GB/s"
 FLUSH_BYTES = 256 << 20
-TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192}
+TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
+                      "shared": 2048}
 
 
 def parse_args():
@@ -62,7 +63,32 @@ def build_metadata(w):
     return lens, tables, width
 
 
-def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0):
+def build_shared_step(w):
+    """Parallel-sampling state built by the library's block manager: prompts,
+    forks, each sample's own tokens (with the copies they caused), then this
+    step's token of every sample.  Returns lens, tables, width, the step's
+    slots and copy pairs, and the copies made while building the state."""
+    import paged_kv_cache_117_gb300 as pkv
+    plan = wl.shared_prefix_plan(w)
+    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    S = plan.prompts * plan.samples
+    setup = []
+    for p in range(plan.prompts):
+        root = p * plan.samples
+        bm.add_sequence(root)
+        bm.append_tokens(root, plan.prompt_len)
+        for i in range(1, plan.samples):
+            bm.fork(root, root + i)
+    for s in range(S):
+        _, pairs = bm.append_tokens(s, plan.own[s])
+        setup += pairs.tolist()
+    slots, pairs = bm.append(range(S))
+    tables, lens = zip(*(bm.table(s) for s in range(S)))
+    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    return list(lens), [list(t) for t in tables], width, slots, pairs, setup
+
+
+def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0, tables=None):
     """Bytes the step must move at minimum: every valid K/V row of every
     (sequence, KV head) once, q, the used block-table entries, lengths, the
     output, the split-context records (written once and read back once), the
@@ -78,8 +104,15 @@ def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0):
     write = S * Hkv * D * es * 2 * 2 + S * 8
     block_bytes = B * Hkv * D * es
     copy = n_pairs * block_bytes * 2 * 2 + n_pairs * 16
-    return {"kv": kv, "attention": attention, "records": 2 * rec, "write": write,
-            "copy": copy, "step": attention + write + copy}
+    res = {"kv": kv, "attention": attention, "records": 2 * rec, "write": write,
+           "copy": copy, "step": attention + write + copy}
+    if tables is not None:   # distinct (block, KV head, valid slot) rows, for shared blocks
+        seen = {}
+        for t, L in zip(tables, lens):
+            for j, b in enumerate(t[: -(-L // B)]):
+                seen[b] = max(seen.get(b, 0), min(B, L - j * B))
+        res["kv_unique"] = sum(seen.values()) * Hkv * D * es * 2
+    return res
 
 
 def peak_hbm():
@@ -119,10 +152,17 @@ def measured_traffic(workload, partition_tokens):
 
 
 def workload_desc(w, width):
-    lk = {"lognormal": "lognormal lengths (median %g, sigma %g, clipped to [%d, %d])",
-          "uniform": "uniform lengths in [%d, %d]", "fixed": "fixed lengths"}[w.lens_kind]
-    lk = lk % w.lens_args if w.lens_kind != "fixed" else \
-        f"fixed lengths {sorted(set(w.lens_args))}"
+    if w.lens_kind == "shared":
+        pr, plen, n, lo, hi = w.lens_args
+        lk = (f"{pr} prompts of {plen} tokens x {n} samples sharing the prompt blocks, "
+              f"{lo}-{hi} own tokens per sample (samples 0 and 1 of each prompt: 0), "
+              f"copy-on-write of the shared partial block in the step; shared blocks are "
+              f"read once per sharer (L2 reuse across sharers, not graded)")
+    elif w.lens_kind == "fixed":
+        lk = f"fixed lengths {sorted(set(w.lens_args))}"
+    else:
+        lk = {"lognormal": "lognormal lengths (median %g, sigma %g, clipped to [%d, %d])",
+              "uniform": "uniform lengths in [%d, %d]"}[w.lens_kind] % w.lens_args
     return (f"{w.name}: {w.num_seqs} seqs, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
             f"head_dim {w.head_dim}, {str(w.dtype).replace('torch.', '')}, block {w.block_size}, "
             f"{lk}, {w.num_blocks}-block pool, blocks scattered by a seeded permutation, "
@@ -251,20 +291,28 @@ def run_native(a, world, rank, local):
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[a.workload]
     pt = w.partition_tokens if a.partition is None else a.partition
-    lens, tables, width = build_metadata(w)
+    k, v = wl.make_pool_chunked(w, dev)
+    if w.lens_kind == "shared":
+        lens, tables, width, slots_cpu, pairs_cpu, setup = build_shared_step(w)
+        if setup:   # copies made while the samples added their own tokens
+            pkv.paged_block_copy(k, v, torch.tensor(setup, dtype=torch.int64, device=dev))
+    else:
+        lens, tables, width = build_metadata(w)
+        pairs_cpu = torch.zeros((0, 2), dtype=torch.int64)
     tab_cpu = wl.pad_tables(tables, width)
     lens_cpu = torch.tensor(lens, dtype=torch.int32)
-    slots_cpu = pkv.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size)
-    k, v = wl.make_pool_chunked(w, dev)
+    if w.lens_kind != "shared":
+        slots_cpu = pkv.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size)
     q, key, value = wl.make_step_inputs(w, dev)
     tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
-    pairs = torch.zeros((0, 2), dtype=torch.int64, device=dev)
+    pairs = pairs_cpu.to(dev)
     out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
     nws = pkv.paged_attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
                                               width * w.block_size, pt)
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0])
+    nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0],
+                               tables if w.lens_kind == "shared" else None)
     # block copy (when there are pairs) + KV write + work list + attention
     launches_per_step = (1 if pairs.shape[0] else 0) + 1 + 2
 
@@ -325,17 +373,18 @@ def run_native(a, world, rank, local):
     # end to end: each step's inputs (q, new K/V rows, block tables, lengths,
     # slot mapping) arrive in one pinned host staging buffer and go to the
     # device in one copy; the result comes back in one copy
-    parts = [q, key, value, tab, lens_t, slots]
+    parts = [q, key, value, tab, lens_t, slots, pairs]
     sizes = [t.numel() * t.element_size() for t in parts]
     offs = [0]
     for n in sizes:
         offs.append(offs[-1] + (n + 255) // 256 * 256)
     h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
     d_in = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
-    for t, o, n in zip((q, key, value, tab_cpu, lens_cpu, slots_cpu), offs, sizes):
-        h_in[o:o + n].copy_(t.cpu().contiguous().view(torch.uint8).view(-1))
+    for t, o, n in zip((q, key, value, tab_cpu, lens_cpu, slots_cpu, pairs_cpu), offs, sizes):
+        if n:
+            h_in[o:o + n].copy_(t.cpu().contiguous().view(torch.uint8).view(-1))
     views = [d_in[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
-    e_q, e_key, e_val, e_tab, e_lens, e_slots = views
+    e_q, e_key, e_val, e_tab, e_lens, e_slots, e_pairs = views
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(sizes)
     d2h = h_out.numel() * h_out.element_size()
@@ -343,7 +392,7 @@ def run_native(a, world, rank, local):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         if pairs.shape[0]:
-            pkv.paged_block_copy(k, v, pairs)
+            pkv.paged_block_copy(k, v, e_pairs)
         pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
         pkv.paged_attention_decode(out, e_q, k, v, e_tab, e_lens, w.scale, partition_tokens=pt,
                                    workspace=ws)
@@ -401,7 +450,10 @@ def run_reference(a, world, rank, local):
     if rank != 0:
         return None
     w = wl.WORKLOADS[a.workload]
-    lens, tables, width = build_metadata(w)
+    if w.lens_kind == "shared":
+        lens, tables, width, slot_t, _, _ = build_shared_step(w)
+    else:
+        lens, tables, width = build_metadata(w)
     # inputs with the same distributions, generated on the CPU for just the
     # blocks the sample reads (no GPU needed)
     nseq = max(1, min(w.num_seqs, 4))
@@ -414,7 +466,8 @@ def run_reference(a, world, rank, local):
     tab_cpu = wl.pad_tables(tables, width)
     lens_cpu = torch.tensor(lens, dtype=torch.int32)
     import paged_kv_cache_117_gb300.binding as bnd
-    slots = bnd.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size).tolist()
+    slots = (slot_t.tolist() if w.lens_kind == "shared"
+             else bnd.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size).tolist())
     times, nbytes, threads = [], 0, torch.get_num_threads()
     for i in range(max(3, a.warmup) + a.steps):
         dt, b, threads = oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value,

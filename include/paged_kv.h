@@ -63,7 +63,8 @@ typedef enum {
   PKV_ERR_ALIAS = 5,     /* buffers that must be distinct overlap */
   PKV_ERR_CUDA = 6,      /* a CUDA runtime / driver call failed */
   PKV_ERR_WORKSPACE = 7, /* workspace missing or too small */
-  PKV_ERR_ALIGN = 8      /* a pointer is not aligned as required */
+  PKV_ERR_ALIGN = 8,     /* a pointer is not aligned as required */
+  PKV_ERR_NO_BLOCKS = 9  /* the block manager has too few free blocks */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
@@ -215,6 +216,59 @@ pkv_status paged_attention_decode_noalloc(
     int max_blocks, const int32_t *context_lens, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     int num_blocks, float scale, int partition_tokens, pkv_stream_t stream);
+
+/*
+ * Host-side block manager (no device memory involved): on-demand block
+ * allocation, reference counts and copy-on-write, producing the block tables,
+ * slot mapping and copy pairs that the calls above consume.
+ *
+ * The rules follow the pages: a sequence takes a new block only when its last
+ * one is full ("PagedAttention" (tensortonic), section 3; "PagedAttention and
+ * vLLM ...", Step 3); free blocks are handed out first in, first out and come
+ * back when their count reaches zero ("vLLM's PagedAttention ...", sections
+ * 2.4 and 7); forking copies the block table and raises the counts; a writer
+ * whose last block is shared (count > 1) copies it to a fresh block first,
+ * while a writer that finds the count at one writes in place ("PagedAttention
+ * and vLLM ...", Step 4).  Not thread-safe: one manager, one thread at a time.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of num_blocks blocks of block_size tokens.  free_order (may be
+ * NULL = ascending) is the order in which free blocks are first handed out; it
+ * must be a permutation of 0..num_blocks-1.  Returns NULL on invalid
+ * arguments or allocation failure.  Release with pkv_bm_destroy. */
+pkv_block_manager *pkv_bm_create(int num_blocks, int block_size,
+                                 const int32_t *free_order);
+void pkv_bm_destroy(pkv_block_manager *bm);
+
+/* New empty sequence (PKV_ERR_RANGE if the id exists). */
+pkv_status pkv_bm_add_sequence(pkv_block_manager *bm, int64_t seq);
+/* child shares every block of parent (PKV_ERR_RANGE: unknown parent or
+ * existing child). */
+pkv_status pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child);
+/* Drops the sequence; blocks whose count reaches zero return to the free
+ * queue. */
+pkv_status pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq);
+
+/*
+ * Reserves the next token slot of each of seqs[0..n-1], in that order (a
+ * sequence may appear more than once).  slots[i] = block * block_size +
+ * offset.  Every copy-on-write appends one (src, dst) pair to pairs (room for
+ * n pairs) and *num_pairs receives their count; the copies must run
+ * (paged_block_copy) before the writes.  Refuses with PKV_ERR_NO_BLOCKS,
+ * changing nothing, when the batch needs more blocks than are free.
+ */
+pkv_status pkv_bm_append(pkv_block_manager *bm, const int64_t *seqs, int n,
+                         int64_t *slots, int64_t *pairs, int *num_pairs);
+
+/* Copies up to `capacity` entries of the sequence's block table to out;
+ * *num_blocks receives the table length and *num_tokens its token count. */
+pkv_status pkv_bm_table(const pkv_block_manager *bm, int64_t seq, int32_t *out,
+                        int capacity, int *num_blocks, int64_t *num_tokens);
+
+/* Free blocks, and a block's reference count (-1 on invalid arguments). */
+int pkv_bm_num_free(const pkv_block_manager *bm);
+int pkv_bm_refcount(const pkv_block_manager *bm, int block);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *pkv_status_string(pkv_status status);

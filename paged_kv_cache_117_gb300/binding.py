@@ -34,6 +34,9 @@ EXPORTED_SYMBOLS = (
     "pkv_read_device_flags",
     "pkv_last_error_string",
     "paged_attention_decode_noalloc",
+    "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_fork",
+    "pkv_bm_free_sequence", "pkv_bm_append", "pkv_bm_table", "pkv_bm_num_free",
+    "pkv_bm_refcount",
 )
 
 # Fixed scratch size of paged_attention_decode_noalloc (PKV_NOALLOC_SCRATCH_BYTES).
@@ -80,6 +83,25 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.paged_attention_decode_noalloc.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, ci, ci,
                                                    ci, ci, ci, ci, cf, ci, vp]
     lib.paged_attention_decode_noalloc.restype = ci
+    i64, i32p, i64p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    lib.pkv_bm_create.argtypes = [ci, ci, vp]
+    lib.pkv_bm_create.restype = vp
+    lib.pkv_bm_destroy.argtypes = [vp]
+    lib.pkv_bm_destroy.restype = None
+    lib.pkv_bm_add_sequence.argtypes = [vp, i64]
+    lib.pkv_bm_add_sequence.restype = ci
+    lib.pkv_bm_fork.argtypes = [vp, i64, i64]
+    lib.pkv_bm_fork.restype = ci
+    lib.pkv_bm_free_sequence.argtypes = [vp, i64]
+    lib.pkv_bm_free_sequence.restype = ci
+    lib.pkv_bm_append.argtypes = [vp, vp, ci, vp, vp, ctypes.POINTER(ci)]
+    lib.pkv_bm_append.restype = ci
+    lib.pkv_bm_table.argtypes = [vp, i64, vp, ci, ctypes.POINTER(ci), i64p]
+    lib.pkv_bm_table.restype = ci
+    lib.pkv_bm_num_free.argtypes = [vp]
+    lib.pkv_bm_num_free.restype = ci
+    lib.pkv_bm_refcount.argtypes = [vp, ci]
+    lib.pkv_bm_refcount.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -213,3 +235,75 @@ def decode_slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor,
     blk = tabs.gather(1, (pos // block_size).unsqueeze(1)).squeeze(1)
     slots = blk * block_size + pos % block_size
     return torch.where(lens > 0, slots, torch.full_like(slots, -1))
+
+
+class BlockManager:
+    """The library's host-side block manager (pkv_bm_* in the C ABI): block
+    allocation, reference counts and copy-on-write for one pool."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self._lib = load()
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        order = None
+        if free_order is not None:
+            order = torch.as_tensor(list(free_order), dtype=torch.int32).contiguous()
+            if order.numel() != num_blocks:
+                raise ValueError("free_order must list every block once")
+        self._order = order
+        h = self._lib.pkv_bm_create(int(num_blocks), int(block_size),
+                                    None if order is None else order.data_ptr())
+        if not h:
+            raise ValueError("invalid block manager arguments")
+        self._h = h
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pkv_bm_destroy(h)
+
+    def add_sequence(self, seq: int) -> None:
+        _check("pkv_bm_add_sequence", self._lib.pkv_bm_add_sequence(self._h, int(seq)))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pkv_bm_fork", self._lib.pkv_bm_fork(self._h, int(parent), int(child)))
+
+    def free_sequence(self, seq: int) -> None:
+        _check("pkv_bm_free_sequence", self._lib.pkv_bm_free_sequence(self._h, int(seq)))
+
+    def append(self, seqs):
+        """Next-token slots of ``seqs`` (in order) and the copy-on-write pairs
+        that must run first: (int64 [n] slots, int64 [P, 2] pairs), CPU."""
+        ids = torch.as_tensor(list(seqs), dtype=torch.int64).contiguous()
+        n = ids.numel()
+        slots = torch.empty(n, dtype=torch.int64)
+        pairs = torch.empty((max(n, 1), 2), dtype=torch.int64)
+        npairs = ctypes.c_int(0)
+        st = self._lib.pkv_bm_append(self._h, ids.data_ptr() if n else None, n,
+                                     slots.data_ptr() if n else None, pairs.data_ptr(),
+                                     ctypes.byref(npairs))
+        _check("pkv_bm_append", st)
+        return slots, pairs[: npairs.value].clone()
+
+    def append_tokens(self, seq: int, count: int):
+        """`count` tokens to one sequence: (slots, pairs)."""
+        return self.append([seq] * int(count))
+
+    def table(self, seq: int):
+        """(block table as a list, number of tokens) of one sequence."""
+        nb, nt = ctypes.c_int(0), ctypes.c_int64(0)
+        _check("pkv_bm_table", self._lib.pkv_bm_table(self._h, int(seq), None, 0,
+                                                      ctypes.byref(nb), ctypes.byref(nt)))
+        out = torch.empty(max(nb.value, 1), dtype=torch.int32)
+        _check("pkv_bm_table", self._lib.pkv_bm_table(self._h, int(seq), out.data_ptr(),
+                                                      nb.value, ctypes.byref(nb),
+                                                      ctypes.byref(nt)))
+        return out[: nb.value].tolist(), int(nt.value)
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_bm_num_free(self._h))
+
+    def num_used_blocks(self) -> int:
+        return self.num_blocks - self.num_free()
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_bm_refcount(self._h, int(block)))

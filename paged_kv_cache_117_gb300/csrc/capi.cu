@@ -141,6 +141,7 @@ const char *pkv_status_string(pkv_status s) {
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_ALIGN: return "pointer not aligned as required";
+    case PKV_ERR_NO_BLOCKS: return "too few free blocks";
   }
   return "unknown status";
 }

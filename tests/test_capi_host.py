@@ -13,7 +13,7 @@ from paged_kv_cache_117_gb300 import build as pbuild
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER_DIR = os.path.join(ROOT, "include")
 
-OK, NULL, SHAPE, DTYPE, RANGE, ALIAS, CUDA, WS, ALIGN = range(9)
+OK, NULL, SHAPE, DTYPE, RANGE, ALIAS, CUDA, WS, ALIGN, NO_BLOCKS = range(10)
 F16, BF16, F32 = 0, 1, 2
 
 
@@ -43,8 +43,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
-        assert lib.pkv_status_string(code)
+    for code in range(10):
+        assert lib.pkv_status_string(code) != b"unknown status"
     assert lib.pkv_status_string(99) == b"unknown status"
 
 
