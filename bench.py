@@ -50,6 +50,10 @@ def parse_args():
     ap.add_argument("--cpu-seqs", type=int, default=256,
                     help="sequences in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="layers per step: one K/V pool per layer, shared block tables")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the whole step (all layers) in one CUDA graph and replay it")
     return ap.parse_args()
 
 
@@ -306,15 +310,27 @@ def run_native(a, world, rank, local):
     q, key, value = wl.make_step_inputs(w, dev)
     tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
     pairs = pairs_cpu.to(dev)
+    import dataclasses
+    layers = [(k, v, q, key, value)]
+    for li in range(1, a.layers):   # one pool per layer; one block id = one slot range in all
+        wl_l = dataclasses.replace(w, seed=w.seed + 10 * li)
+        kl, vl = wl.make_pool_chunked(wl_l, dev)
+        if w.lens_kind == "shared" and setup:
+            pkv.paged_block_copy(kl, vl, torch.tensor(setup, dtype=torch.int64, device=dev))
+        layers.append((kl, vl) + tuple(wl.make_step_inputs(wl_l, dev)))
+    outs = [torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
+            for _ in range(a.layers)]
     out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
     nws = pkv.paged_attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
                                               width * w.block_size, pt)
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    wss = [ws] + [torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+                  for _ in range(1, a.layers)]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0],
                                tables if w.lens_kind == "shared" else None)
-    # block copy (when there are pairs) + KV write + work list + attention
-    launches_per_step = (1 if pairs.shape[0] else 0) + 1 + 2
+    # block copy (when there are pairs) + KV write + work list + attention, per layer
+    launches_per_step = a.layers * ((1 if pairs.shape[0] else 0) + 1 + 2)
 
     # CPU-oracle sample: inputs snapshot before any library kernel runs
     cpu = None
@@ -332,15 +348,16 @@ def run_native(a, world, rank, local):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(d0=None, d1=None):
-        if pairs.shape[0]:
-            pkv.paged_block_copy(k, v, pairs)
-        pkv.paged_kv_write(key, value, k, v, slots)
-        if d0 is not None:
-            d0.record(stream)
-        pkv.paged_attention_decode(out, q, k, v, tab, lens_t, w.scale, partition_tokens=pt,
-                                   workspace=ws)
-        if d1 is not None:
-            d1.record(stream)
+        for li, (kl, vl, ql, keyl, vall) in enumerate(layers):
+            if pairs.shape[0]:
+                pkv.paged_block_copy(kl, vl, pairs)
+            pkv.paged_kv_write(keyl, vall, kl, vl, slots)
+            if li == 0 and d0 is not None:
+                d0.record(stream)
+            pkv.paged_attention_decode(outs[li] if li else out, ql, kl, vl, tab, lens_t,
+                                       w.scale, partition_tokens=pt, workspace=wss[li])
+            if li == 0 and d1 is not None:
+                d1.record(stream)
 
     for _ in range(max(3, a.warmup)):
         flush.zero_()
@@ -349,6 +366,12 @@ def run_native(a, world, rank, local):
     assert pkv.read_device_flags(clear=True) == 0
 
     K = a.steps
+    graph = None
+    if a.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
     evs = [(ev(), ev(), ev(), ev()) for _ in range(K)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
@@ -359,13 +382,24 @@ def run_native(a, world, rank, local):
     for s0, s1, d0, d1 in evs:
         flush.zero_()
         s0.record(stream)
-        step(d0, d1)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(d0, d1)
         s1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
     step_ms = sum(s0.elapsed_time(s1) for s0, s1, _, _ in evs) / K
+    if graph is not None:   # layer 0's attention call, timed eagerly for the roofline
+        for _, _, d0, d1 in evs:
+            flush.zero_()
+            d0.record(stream)
+            pkv.paged_attention_decode(out, q, k, v, tab, lens_t, w.scale, partition_tokens=pt,
+                                       workspace=ws)
+            d1.record(stream)
+        torch.cuda.synchronize()
     dec_ms = sum(d0.elapsed_time(d1) for _, _, d0, d1 in evs) / K
     step_ms = max_over_ranks(world, step_ms, dev)
     dec_ms = max_over_ranks(world, dec_ms, dev)
@@ -398,9 +432,11 @@ def run_native(a, world, rank, local):
                                    workspace=ws)
         h_out.copy_(out, non_blocking=True)
 
-    for _ in range(3):
+    if a.layers != 1:   # the end-to-end leg times the single-layer step only
+        e2e_step = None
+    for _ in range(3 if e2e_step else 0):
         e2e_step()
-    e2e_evs = [(ev(), ev()) for _ in range(K)]
+    e2e_evs = [(ev(), ev()) for _ in range(K if e2e_step else 0)]
     barrier(world)
     torch.cuda.synchronize()
     for e0, e1 in e2e_evs:
@@ -409,12 +445,13 @@ def run_native(a, world, rank, local):
         e2e_step()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(world, sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / K, dev)
+    e2e_ms = (max_over_ranks(world, sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / K, dev)
+              if e2e_evs else None)
     assert pkv.read_device_flags(clear=True) == 0
 
     peak, peak_kind = peak_hbm()
     achieved = nbytes["attention"] / (dec_ms * 1e-3) / 1e9
-    value_gbs = world * nbytes["step"] / (step_ms * 1e-3) / 1e9
+    value_gbs = world * a.layers * nbytes["step"] / (step_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
@@ -424,6 +461,7 @@ def run_native(a, world, rank, local):
         "config": {"workload": workload_desc(w, width), "partition_tokens": pt,
                    "out_dtype": str(out.dtype).replace("torch.", ""),
                    "l2": "flushed before every step (256 MiB write, outside the timed span)",
+                   "layers": a.layers, "cuda_graph": bool(a.graph),
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "pct_of_peak": round(100 * value_gbs / world / peak, 1),
         "seq_steps_per_s": round(world * w.num_seqs / (step_ms * 1e-3), 1),
@@ -434,9 +472,9 @@ def run_native(a, world, rank, local):
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": measured_traffic(w.name, pt)},
-        "e2e": {"value": round(world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": ({"value": round(world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h} if e2e_ms else None),
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
