@@ -35,7 +35,8 @@ METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 UNIT = "GB/s"
 FLUSH_BYTES = 256 << 20
 TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
-                      "shared": 2048}
+                      "shared": 2048, "beam": 2048}
+SHARING = ("shared", "beam")   # workloads whose sequences share blocks
 
 
 def parse_args():
@@ -90,6 +91,44 @@ def build_shared_step(w):
     tables, lens = zip(*(bm.table(s) for s in range(S)))
     width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
     return list(lens), [list(t) for t in tables], width, slots, pairs, setup
+
+
+def build_beam_step(w):
+    """Beam-search state built by the library's block manager: prompts, beam
+    forks, then every history step's forks, frees and one token per surviving
+    beam.  Returns lens, tables, width, the measured step's slots and copy
+    pairs, and the history as (pairs, slots) per step (to replay on a pool)."""
+    import paged_kv_cache_117_gb300 as pkv
+    plan = wl.beam_plan(w)
+    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    R, W = plan.requests, plan.width
+    for r in range(R):
+        bm.add_sequence(r * W)
+        bm.append_tokens(r * W, plan.prompt_len)
+        for i in range(1, W):
+            bm.fork(r * W, r * W + i)
+    hist = []
+    for st in wl.beam_schedule(plan):
+        for parent, child in st.forks:
+            bm.fork(parent, child)
+        for sq in st.frees:
+            bm.free_sequence(sq)
+        slots, pairs = bm.append(st.order)
+        hist.append((pairs, slots))
+    tables, lens = zip(*(bm.table(sq) for sq in st.order))
+    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    pairs, slots = hist.pop()
+    return list(lens), [list(t) for t in tables], width, slots, pairs, hist
+
+
+def replay_beam_history(w, k, v, hist, dev):
+    """Runs the history's copies and writes on one pool through the library."""
+    import paged_kv_cache_117_gb300 as pkv
+    for t, (pairs, slots) in enumerate(hist):
+        key, val = wl.make_rows(w, t, slots.numel(), dev)
+        if pairs.shape[0]:
+            pkv.paged_block_copy(k, v, pairs.to(dev))
+        pkv.paged_kv_write(key, val, k, v, slots.to(dev))
 
 
 def algorithmic_bytes(w, lens, width, pt, out_es, n_pairs=0, tables=None):
@@ -162,6 +201,12 @@ def workload_desc(w, width):
               f"{lo}-{hi} own tokens per sample (samples 0 and 1 of each prompt: 0), "
               f"copy-on-write of the shared partial block in the step; shared blocks are "
               f"read once per sharer (L2 reuse across sharers, not graded)")
+    elif w.lens_kind == "beam":
+        rq, plen, n, c, steps = w.lens_args
+        lk = (f"beam search: {rq} prompts of {plen} tokens x {n} beams, {c} seeded-score "
+              f"candidates per beam, top {n} survive; {steps} steps of forks, frees, "
+              f"copy-on-write copies and writes replayed on the pool before the measured "
+              f"step (copies + write + attention)")
     elif w.lens_kind == "fixed":
         lk = f"fixed lengths {sorted(set(w.lens_args))}"
     else:
@@ -296,16 +341,20 @@ def run_native(a, world, rank, local):
     w = wl.WORKLOADS[a.workload]
     pt = w.partition_tokens if a.partition is None else a.partition
     k, v = wl.make_pool_chunked(w, dev)
+    hist = None
     if w.lens_kind == "shared":
         lens, tables, width, slots_cpu, pairs_cpu, setup = build_shared_step(w)
         if setup:   # copies made while the samples added their own tokens
             pkv.paged_block_copy(k, v, torch.tensor(setup, dtype=torch.int64, device=dev))
+    elif w.lens_kind == "beam":
+        lens, tables, width, slots_cpu, pairs_cpu, hist = build_beam_step(w)
+        replay_beam_history(w, k, v, hist, dev)
     else:
         lens, tables, width = build_metadata(w)
         pairs_cpu = torch.zeros((0, 2), dtype=torch.int64)
     tab_cpu = wl.pad_tables(tables, width)
     lens_cpu = torch.tensor(lens, dtype=torch.int32)
-    if w.lens_kind != "shared":
+    if w.lens_kind not in SHARING:
         slots_cpu = pkv.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size)
     q, key, value = wl.make_step_inputs(w, dev)
     tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
@@ -317,6 +366,8 @@ def run_native(a, world, rank, local):
         kl, vl = wl.make_pool_chunked(wl_l, dev)
         if w.lens_kind == "shared" and setup:
             pkv.paged_block_copy(kl, vl, torch.tensor(setup, dtype=torch.int64, device=dev))
+        if hist is not None:
+            replay_beam_history(wl_l, kl, vl, hist, dev)
         layers.append((kl, vl) + tuple(wl.make_step_inputs(wl_l, dev)))
     outs = [torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
             for _ in range(a.layers)]
@@ -328,7 +379,7 @@ def run_native(a, world, rank, local):
                   for _ in range(1, a.layers)]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0],
-                               tables if w.lens_kind == "shared" else None)
+                               tables if w.lens_kind in SHARING else None)
     # block copy (when there are pairs) + KV write + work list + attention, per layer
     launches_per_step = a.layers * ((1 if pairs.shape[0] else 0) + 1 + 2)
 
@@ -490,6 +541,8 @@ def run_reference(a, world, rank, local):
     w = wl.WORKLOADS[a.workload]
     if w.lens_kind == "shared":
         lens, tables, width, slot_t, _, _ = build_shared_step(w)
+    elif w.lens_kind == "beam":
+        lens, tables, width, slot_t, _, _ = build_beam_step(w)
     else:
         lens, tables, width = build_metadata(w)
     # inputs with the same distributions, generated on the CPU for just the
@@ -504,7 +557,7 @@ def run_reference(a, world, rank, local):
     tab_cpu = wl.pad_tables(tables, width)
     lens_cpu = torch.tensor(lens, dtype=torch.int32)
     import paged_kv_cache_117_gb300.binding as bnd
-    slots = (slot_t.tolist() if w.lens_kind == "shared"
+    slots = (slot_t.tolist() if w.lens_kind in SHARING
              else bnd.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size).tolist())
     times, nbytes, threads = [], 0, torch.get_num_threads()
     for i in range(max(3, a.warmup) + a.steps):

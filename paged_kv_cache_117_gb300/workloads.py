@@ -22,6 +22,8 @@ The five workloads follow the shapes the pages use for their examples:
                   Model Inference", section 2.1).
 * ``shared``   -- parallel sampling from shared prompts ("PagedAttention and
                   vLLM ...", Step 4): 16 prompts of 1,000 tokens, 8 samples each.
+* ``beam``     -- beam search over shared prompts (same Step 4): 32 prompts of
+                  1,000 tokens, 8 beams each, seeded scores in place of a model.
 
 The pages measure on ShareGPT/Alpaca traces; none is used or reproduced here.
 Lengths come from the seeded distributions below instead.
@@ -30,7 +32,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field, replace
-from typing import List, Optional, Sequence
+from typing import List, Optional, Sequence, Tuple
 
 import torch
 
@@ -47,7 +49,7 @@ class Workload:
     dtype: torch.dtype
     partition_tokens: int          # 0 = one partition per sequence
     seed: int
-    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared"
+    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam"
     lens_args: tuple = field(default_factory=tuple)
 
     @property
@@ -75,7 +77,16 @@ QWEN72B = Workload("qwen72b", 32, 64, 8, 128, 16, 20_480, torch.bfloat16, 512, 1
 SHARED = Workload("shared", 128, 32, 8, 128, 16, 4_096, torch.bfloat16, 512, 122,
                   "shared", (16, 1000, 8, 0, 200))
 
-WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED)}
+# Beam search over shared prompts ("PagedAttention and vLLM ...", Step 4, beam
+# search): 32 prompts of 1,000 tokens, 8 beams each, 20 decode steps before the
+# measured one (so that the measured token lands in a partly filled block and
+# copy-on-write copies happen in it).  Scores come from a seeded generator
+# (there is no model): every beam proposes 2 continuations and the 8
+# best-scoring ones survive.
+BEAM = Workload("beam", 256, 32, 8, 128, 16, 8_192, torch.bfloat16, 512, 123,
+                "beam", (32, 1000, 8, 2, 20))
+
+WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM)}
 
 
 def scaled(w: Workload, num_seqs: int, max_len: Optional[int] = None,
@@ -211,3 +222,76 @@ def scatter_block_tables(lens: Sequence[int], block_size: int,
         tables.append([int(b) for b in order[pos:pos + nb]])
         pos += nb
     return tables
+
+
+@dataclass(frozen=True)
+class BeamPlan:
+    requests: int
+    prompt_len: int
+    width: int
+    cands: int
+    # parents[t][r] = for step t and request r, the parent beam index (0..width-1)
+    # of each of the `width` survivors, in survivor order
+    parents: List[List[List[int]]]
+
+
+def beam_plan(w: Workload, steps: Optional[int] = None) -> BeamPlan:
+    requests, prompt_len, width, cands, n_steps = w.lens_args
+    if steps is not None:
+        n_steps = steps
+    g = _gen(w.seed)
+    parents = []
+    for _ in range(n_steps + 1):            # history steps + the measured step
+        per_req = []
+        for _ in range(requests):
+            scores = torch.rand(width * cands, generator=g, dtype=torch.float64)
+            best = torch.topk(scores, width).indices.tolist()
+            per_req.append([b // cands for b in best])
+        parents.append(per_req)
+    return BeamPlan(requests, prompt_len, width, cands, parents)
+
+
+@dataclass(frozen=True)
+class BeamStep:
+    forks: List[Tuple[int, int]]    # (parent sequence, child sequence), in order
+    frees: List[int]                # pruned sequences, freed after the forks
+    order: List[int]                # surviving sequences, request-major; one token each
+
+
+def beam_schedule(plan: BeamPlan) -> List[BeamStep]:
+    """Sequence-level bookkeeping of a beam plan.  Request r starts as beam
+    sequences r*width .. r*width+width-1, all forked from r*width after its
+    prompt.  In a step, a parent's first surviving child keeps the parent's
+    sequence id, every further child is a fork with a fresh id, and parents
+    with no surviving child are freed."""
+    R, W = plan.requests, plan.width
+    beams = [[r * W + i for i in range(W)] for r in range(R)]
+    next_id = R * W
+    out = []
+    for par_t in plan.parents:
+        forks, frees = [], []
+        for r in range(R):
+            old, new, used = beams[r], [], set()
+            for p in par_t[r]:
+                if p in used:
+                    forks.append((old[p], next_id))
+                    new.append(next_id)
+                    next_id += 1
+                else:
+                    used.add(p)
+                    new.append(old[p])
+            frees += [sq for p, sq in enumerate(old) if p not in used]
+            beams[r] = new
+        out.append(BeamStep(forks, frees, [sq for b in beams for sq in b]))
+    return out
+
+
+def make_rows(w: Workload, step: int, n: int, device="cpu"):
+    """New key/value rows [n, Hkv, D] of history step `step`, N(0,1)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 5000 + step)
+    key = torch.randn((n, w.num_kv_heads, w.head_dim), generator=g, device=device,
+                      dtype=torch.float32).to(w.dtype)
+    value = torch.randn((n, w.num_kv_heads, w.head_dim), generator=g, device=device,
+                        dtype=torch.float32).to(w.dtype)
+    return key, value

@@ -173,3 +173,48 @@ def assert_close_to_oracle(gpu_out: torch.Tensor, ref64: torch.Tensor, atol=2e-3
     bad = (err > bound)
     assert not bad.any(), f"{int(bad.sum())} elements beyond max(atol, 1 ulp); max err {err.max():.3e}"
     return err.max().item() if err.numel() else 0.0
+
+
+# ---- beam search -------------------------------------------------------------
+
+@dataclass
+class BeamHistory:
+    w: wl.Workload
+    steps: list            # per step: (pairs, slots, order)
+    lens: List[int]        # final beams (in final order), after the last step
+    tables: List[List[int]]
+    width: int
+
+
+def plan_beam(w: wl.Workload, steps: Optional[int] = None, width: Optional[int] = None) -> BeamHistory:
+    """Beam-search history on the oracle's block manager: prompts, then for
+    every step the survivors' forks, the pruned beams' frees and one token per
+    surviving beam (with the copy-on-write pairs it causes)."""
+    plan = wl.beam_plan(w, steps)
+    bm = BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    R, W = plan.requests, plan.width
+    for r in range(R):
+        root = r * W
+        bm.add_sequence(root)
+        bm.append_tokens(root, plan.prompt_len)
+        for i in range(1, W):
+            bm.fork(root, r * W + i)
+    hist = []
+    for st in wl.beam_schedule(plan):
+        for parent, child in st.forks:
+            bm.fork(parent, child)
+        for sq in st.frees:
+            bm.free_sequence(sq)
+        slots, pairs = [], []
+        for sq in st.order:
+            slot, cow = bm.append(sq)
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(cow)
+        hist.append((pairs, slots, st.order))
+        bm.check_invariants()
+    order = hist[-1][2]
+    tables = [list(bm.tables[sq]) for sq in order]
+    lens = [bm.lens[sq] for sq in order]
+    need = max(len(t) for t in tables)
+    return BeamHistory(w, hist, lens, tables, width or need)

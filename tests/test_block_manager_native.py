@@ -185,3 +185,21 @@ def test_bench_shared_step_matches_oracle_plan():
     assert slots.tolist() == plan.slots
     assert pairs.tolist() == [list(p) for p in plan.step_pairs] and len(plan.step_pairs) == 16
     assert setup == [list(p) for p in plan.setup_pairs]
+
+
+def test_bench_beam_step_matches_oracle_plan():
+    """Beam search: the benchmark's history (library manager) and the parity
+    tests' history (oracle manager) agree step by step."""
+    import bench
+    from paged_kv_cache_117_gb300 import workloads as wl
+    from tests import gpu_harness as gh
+    w = wl.BEAM
+    lens, tables, width, slots, pairs, hist = bench.build_beam_step(w)
+    ref = gh.plan_beam(w)
+    assert lens == ref.lens and tables == ref.tables and width >= ref.width
+    assert len(hist) + 1 == len(ref.steps)
+    for (p, s), (rp, rs, _) in zip(hist + [(pairs, slots)], ref.steps):
+        assert p.tolist() == [list(x) for x in rp]
+        assert s.tolist() == rs
+    assert len(ref.steps[-1][0]) > 0              # the measured step copies blocks
+    assert sum(len(p) for p, _, _ in ref.steps) > 1000
