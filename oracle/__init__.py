@@ -15,7 +15,11 @@ Contents, each written from the pages' description:
 * ``paged_ops`` -- the per-step K/V slot write, the block copy, and decode
   attention over the block table in fp64 ("PagedAttention and vLLM ...",
   Step 5; "PagedAttention" (tensortonic), section 5; the block-wise attention
-  equation in "PagedAttention: Virtual Memory for the KV Cache").
+  equation in "PagedAttention: Virtual Memory for the KV Cache"), and
+  multi-query attention for chunked prefill mixed with decode
+  (``attend_chunked``: each query attends causally to its own sequence's
+  positions up to its own; "Paging the KV Cache Like an OS", continuous
+  batching and chunked prefill).
 * ``sizing`` -- KV bytes per token and per block ("PagedAttention: Virtual
   Memory for the KV Cache", memory-bound section; "Batching and
   PagedAttention", bytes-per-block formula).

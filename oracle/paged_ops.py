@@ -117,3 +117,48 @@ def attend_contiguous(q: torch.Tensor, keys: List[torch.Tensor],
             out[s, h * G:(h + 1) * G] = attend_one(q[s, h * G:(h + 1) * G],
                                                    keys[s][:, h], values[s][:, h], scale)
     return out
+
+
+def query_positions(context_len: int, num_queries: int) -> List[int]:
+    """Positions of a chunk's queries: the sequence's last ``num_queries``
+    tokens, so query i sits at context_len - num_queries + i."""
+    if num_queries < 0 or num_queries > context_len:
+        raise ValueError("a chunk cannot hold more queries than the sequence has tokens")
+    return [context_len - num_queries + i for i in range(num_queries)]
+
+
+def attend_chunked(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   block_tables, context_lens, query_start, scale: float) -> torch.Tensor:
+    """Multi-query attention over a paged context: chunked prefill, and decode
+    as its one-query case ("Paging the KV Cache Like an OS", continuous
+    batching: a long prompt is processed in chunks over several passes, each
+    filling a few blocks, interleaved with other sequences' decode steps).
+
+    q holds num_tokens query rows [num_tokens, Hq, D], packed by sequence:
+    sequence s owns rows query_start[s] .. query_start[s+1]-1, its last n_s
+    positions (their keys and values are already in the cache, so
+    context_lens[s] = L_s counts them).  The query at position p attends to
+    positions 0..p of its own sequence -- ordinary causal attention, which is
+    what processing a prompt in pieces must reproduce.  float64
+    [num_tokens, Hq, D]."""
+    T, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    scale = float(torch.tensor(scale, dtype=torch.float32))   # the fp32 value
+    tables = block_tables.tolist() if torch.is_tensor(block_tables) else block_tables
+    lens = context_lens.tolist() if torch.is_tensor(context_lens) else context_lens
+    starts = query_start.tolist() if torch.is_tensor(query_start) else query_start
+    assert starts[0] == 0 and starts[-1] == T and len(starts) == len(lens) + 1
+    out = torch.zeros((T, Hq, D), dtype=torch.float64)
+    for s in range(len(lens)):
+        L = int(lens[s])
+        r0, n = int(starts[s]), int(starts[s + 1]) - int(starts[s])
+        pos = query_positions(L, n)
+        keys = gather_logical(k_cache, tables[s], L)
+        vals = gather_logical(v_cache, tables[s], L)
+        for i, p in enumerate(pos):
+            for h in range(Hkv):
+                out[r0 + i, h * G:(h + 1) * G] = attend_one(
+                    q[r0 + i, h * G:(h + 1) * G], keys[: p + 1, h], vals[: p + 1, h], scale)
+    return out
