@@ -10,6 +10,8 @@
  *                           the block manager assigned ("reshape and cache")
  *   paged_block_copy        the batched copy-on-write block copy
  *   paged_attention_decode  single-query attention over the paged context
+ *   paged_attention_chunked multi-query attention over the paged context:
+ *                           chunked prefill and decode in one batch
  *
  * Sources for what each call computes: "PagedAttention and vLLM: Paging the
  * KV Cache Like an OS" (vidyal.ai), Step 5, the three kernels (write, read and
@@ -165,6 +167,50 @@ pkv_status paged_attention_decode(
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     int num_blocks, float scale, int partition_tokens, void *workspace,
     size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * paged_attention_chunked -- multi-query attention over the paged context:
+ * chunks of prompts (chunked prefill) and decode tokens in one batch.
+ *
+ * "Paging the KV Cache Like an OS" (continuous batching; chunked prefill): a
+ * long prompt is split into chunks processed over several passes, each
+ * filling a few blocks allocated on demand, interleaved with other
+ * sequences' decode steps.  Sequence s contributes the n_s = query_start[s+1]
+ * - query_start[s] query rows q[query_start[s] .. query_start[s+1]-1], its
+ * LAST n_s positions: with L_s = context_lens[s] (which counts them), row i
+ * sits at position p = L_s - n_s + i and attends to positions 0..p of its own
+ * sequence (causal attention; a decode token is the case n_s = 1):
+ *   out[row, hq, :] = sum_{t <= p} softmax_t(scale * q[row, hq, :] . K_t) V_t
+ * The chunk's keys and values must already be in the pool (paged_kv_write of
+ * its n_s tokens earlier on the same stream).
+ *
+ *   out            [num_tokens, num_q_heads, head_dim] of out_dtype (F32, F16
+ *                  or BF16), 16-byte aligned
+ *   q              [num_tokens, num_q_heads, head_dim], cache dtype
+ *   block_tables   int32 [num_seqs, max_blocks]
+ *   context_lens   int32 [num_seqs]; L_s >= n_s
+ *   query_start    int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
+ *                  query_start[num_seqs] = num_tokens
+ *   max_query_len  an upper bound of every n_s (sizes the launch)
+ *
+ * Extra shape limits: num_q_heads / num_kv_heads <= 128; block_size 8, 16 or
+ * 32 (the tiles are staged in 128-byte-swizzled shared memory whose 1 KiB
+ * atoms a 4-token block cannot fill).  Accuracy: scores
+ * and the online softmax in fp32; P enters P.V as a 16-bit hi + lo pair.
+ * Device-side checks: a sequence whose query_start entries are out of order
+ * or past num_tokens, whose n_s exceeds max_query_len, or whose L_s < n_s is
+ * skipped (its rows are left untouched) and flagged PKV_FLAG_LEN_RANGE; L_s
+ * past the table is clamped and flagged; bad block ids are read as zeros and
+ * flagged PKV_FLAG_BLOCK_RANGE.  No workspace: one launch, one CTA per
+ * (query tile of 128 / G tokens, sequence, KV head).
+ */
+pkv_status paged_attention_chunked(
+    void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
+    const void *v_cache, pkv_dtype dtype, const int32_t *block_tables,
+    int max_blocks, const int32_t *context_lens, const int32_t *query_start,
+    int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, pkv_stream_t stream);
 
 /*
  * Scratch bytes paged_attention_decode needs, with

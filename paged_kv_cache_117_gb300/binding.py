@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "pkv_read_device_flags",
     "pkv_last_error_string",
     "paged_attention_decode_noalloc",
+    "paged_attention_chunked",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_fork",
     "pkv_bm_free_sequence", "pkv_bm_append", "pkv_bm_table", "pkv_bm_num_free",
     "pkv_bm_refcount",
@@ -84,6 +85,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                    ci, ci, ci, ci, cf, ci, vp]
     lib.paged_attention_decode_noalloc.restype = ci
     i64, i32p, i64p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    lib.paged_attention_chunked.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, vp, ci, ci, ci,
+                                            ci, ci, ci, ci, ci, ctypes.c_float, vp]
+    lib.paged_attention_chunked.restype = ci
     lib.pkv_bm_create.argtypes = [ci, ci, vp]
     lib.pkv_bm_create.restype = vp
     lib.pkv_bm_destroy.argtypes = [vp]
@@ -214,6 +218,34 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
         _ptr(context_lens), S, Hq, Hkv, D, B, N, float(scale), int(partition_tokens),
         _stream(stream))
     _check("paged_attention_decode_noalloc", st)
+    return out
+
+
+def paged_attention_chunked(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                            scale, max_query_len=None, stream=None):
+    """Multi-query attention (chunked prefill and decode in one batch): out
+    [T, Hq, D] from q [T, Hq, D], rows packed by sequence as query_start
+    (int32 [S + 1]) says, each sequence's rows being its last positions.
+    ``max_query_len`` bounds every sequence's row count; when omitted it is
+    read from query_start (a device-to-host copy)."""
+    _need_cuda("paged_attention_chunked", out, q, k_cache, v_cache, block_tables, context_lens,
+               query_start)
+    N, B, Hkv, D = _cache_dims(k_cache)
+    T, Hq, _ = (int(x) for x in q.shape)
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32
+            or query_start.dtype != torch.int32):
+        raise ValueError("block_tables, context_lens and query_start must be int32")
+    S = int(context_lens.shape[0])
+    if int(query_start.shape[0]) != S + 1:
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if S else 0
+    st = load().paged_attention_chunked(
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(context_lens), _ptr(query_start), S, T, int(max_query_len), Hq, Hkv, D, B, N,
+        float(scale), _stream(stream))
+    _check("paged_attention_chunked", st)
     return out
 
 

@@ -303,6 +303,95 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention_decode launch");
 }
 
+pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q,
+                                   const void *k_cache, const void *v_cache, pkv_dtype dtype,
+                                   const int32_t *block_tables, int max_blocks,
+                                   const int32_t *context_lens, const int32_t *query_start,
+                                   int num_seqs, int num_tokens, int max_query_len,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, float scale,
+                                   pkv_stream_t stream) {
+  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
+    return PKV_ERR_RANGE;
+  if (!supported_cache_dtype(dtype)) return PKV_ERR_DTYPE;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16)
+    return PKV_ERR_DTYPE;
+  if (!supported_head_dim(head_dim) || !supported_block(block_size)) return PKV_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 128) return PKV_ERR_SHAPE;
+  if (block_size < 8) return PKV_ERR_SHAPE;   // a block's box must fill whole swizzle atoms
+  if ((long long)max_blocks * block_size > INT_MAX) return PKV_ERR_RANGE;
+  if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+  if (max_query_len > num_tokens) return PKV_ERR_RANGE;
+  const int tile_tokens = 128 / group;
+  const long long qtiles = ceil_div_ll(max_query_len, tile_tokens);
+  if (qtiles * num_seqs * num_kv_heads > INT_MAX) return PKV_ERR_RANGE;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+    return PKV_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4))
+    return PKV_ERR_ALIGN;
+  const size_t pool = (size_t)num_blocks * block_size * num_kv_heads * head_dim * 2;
+  const size_t rows = (size_t)num_tokens * num_q_heads * head_dim;
+  const size_t out_sz = rows * dtype_bytes(out_dtype), q_sz = rows * 2;
+  if (overlap(k_cache, pool, v_cache, pool) || overlap(out, out_sz, q, q_sz) ||
+      overlap(out, out_sz, k_cache, pool) || overlap(out, out_sz, v_cache, pool) ||
+      overlap(out, out_sz, block_tables, (size_t)num_seqs * max_blocks * 4) ||
+      overlap(out, out_sz, context_lens, (size_t)num_seqs * 4) ||
+      overlap(out, out_sz, query_start, (size_t)(num_seqs + 1) * 4))
+    return PKV_ERR_ALIAS;
+
+  CUtensorMap kmap, vmap, qmap;
+  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    return cuda_fail_msg("cuTensorMapEncodeTiled failed for the KV pool");
+  {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cuda_fail_msg("cuTensorMapEncodeTiled unavailable");
+    // q as [tokens][heads][dims]; one box = 64 dims x the group's heads x
+    // 128 / group tokens (128 rows of 128 bytes, 128B-swizzled)
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)tile_tokens};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    memset(&qmap, 0, sizeof(qmap));
+    const CUtensorMapDataType t =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (fn(&qmap, t, 3, const_cast<void *>(q), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cuda_fail_msg("cuTensorMapEncodeTiled failed for q");
+  }
+  unsigned *flags = device_flags();
+  if (!flags) return cuda_fail_msg("device flag word unavailable");
+
+  pkv::ChunkedParams p;
+  p.out = out;
+  p.out_dtype = (int)out_dtype;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.max_blocks = max_blocks;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.tile_tokens = tile_tokens;
+  p.num_qtiles = (int)qtiles;
+  p.max_query_len = max_query_len;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.flags = flags;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      dtype == PKV_BF16 ? pkv::launch_chunked_bf16(qmap, kmap, vmap, p, head_dim, block_size, st)
+                        : pkv::launch_chunked_f16(qmap, kmap, vmap, p, head_dim, block_size, st);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention_chunked launch");
+}
+
 pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear, pkv_stream_t stream) {
   if (!flags_out) return PKV_ERR_NULL;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

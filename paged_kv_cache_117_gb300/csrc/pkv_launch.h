@@ -77,6 +77,35 @@ cudaError_t launch_decode_f16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeParams &p, int head_dim, int block_size,
                               cudaStream_t stream, int *launches);
 
+// Multi-query (chunked prefill) attention: one CTA per (query tile,
+// sequence, KV head).  A query tile is tile_tokens = 128 / group tokens.
+struct ChunkedParams {
+  void *out;                     // [num_tokens, Hq, D]
+  int out_dtype;                 // pkv_dtype
+  const int32_t *block_tables;   // [S, max_blocks]
+  const int32_t *context_lens;   // [S], counting this chunk's tokens
+  const int32_t *query_start;    // [S + 1]
+  int max_blocks;
+  int num_seqs;
+  int num_tokens;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int tile_tokens;
+  int num_qtiles;                // ceil(max_query_len / tile_tokens)
+  int max_query_len;
+  int num_blocks;
+  float scale_log2;
+  unsigned *flags;
+};
+
+cudaError_t launch_chunked_bf16(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, const ChunkedParams &p, int head_dim,
+                                int block_size, cudaStream_t stream);
+cudaError_t launch_chunked_f16(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, const ChunkedParams &p, int head_dim,
+                               int block_size, cudaStream_t stream);
+
 // Launches `kern` with programmatic stream serialization allowed, so that
 // its launch overlaps the tail of the previous kernel on `stream`.  The
 // kernels call griddepcontrol.wait before touching shared data.

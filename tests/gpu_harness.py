@@ -218,3 +218,51 @@ def plan_beam(w: wl.Workload, steps: Optional[int] = None, width: Optional[int] 
     lens = [bm.lens[sq] for sq in order]
     need = max(len(t) for t in tables)
     return BeamHistory(w, hist, lens, tables, width or need)
+
+
+# ---- chunked prefill ---------------------------------------------------------
+
+@dataclass
+class ChunkStep:
+    w: wl.Workload
+    prior: List[int]          # tokens in the cache before the step
+    counts: List[int]         # this step's query tokens per sequence
+    lens: List[int]           # after the step
+    tables: List[List[int]]
+    width: int
+    slots: List[int]          # one per query row, packed by sequence
+    query_start: List[int]
+
+
+def plan_chunked(w: wl.Workload, prior: Sequence[int], counts: Sequence[int],
+                 width: Optional[int] = None) -> ChunkStep:
+    """Sequences that already hold ``prior`` tokens receive ``counts`` new
+    tokens each (a prompt chunk, a decode token, or nothing), through the
+    oracle's block manager."""
+    bm = BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    slots = []
+    for s, (c0, n) in enumerate(zip(prior, counts)):
+        bm.add_sequence(s)
+        bm.append_tokens(s, c0)
+    for s, n in enumerate(counts):
+        new, _ = bm.append_tokens(s, n)
+        slots += list(new)
+    S = len(prior)
+    lens = [bm.lens[s] for s in range(S)]
+    tables = [list(bm.tables[s]) for s in range(S)]
+    need = max(1, max(len(t) for t in tables))
+    qs = [0]
+    for n in counts:
+        qs.append(qs[-1] + n)
+    return ChunkStep(w, list(prior), list(counts), lens, tables, width or need, slots, qs)
+
+
+def unused_slots(step: ChunkStep) -> List[tuple]:
+    """(block, offset) of every pool slot that no sequence's first L_s tokens
+    occupy."""
+    B = step.w.block_size
+    used = set()
+    for t, L in zip(step.tables, step.lens):
+        for pos in range(L):
+            used.add((t[pos // B], pos % B))
+    return [(b, o) for b in range(step.w.num_blocks) for o in range(B) if (b, o) not in used]

@@ -100,6 +100,39 @@ def test_decode_validation(lib):
     assert decode(lib, S=0) == OK           # nothing to do: returns before any CUDA call
 
 
+def chunked(lib, **kw):
+    a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
+             max_blocks=4, lens=fake(5), qs=fake(6), S=2, T=64, maxq=32, Hq=8, Hkv=2, D=128,
+             B=16, N=8, scale=0.1)
+    a.update(kw)
+    return lib.paged_attention_chunked(a["out"], a["out_dt"], a["q"], a["k"], a["v"], a["dt"],
+                                       a["tab"], a["max_blocks"], a["lens"], a["qs"], a["S"],
+                                       a["T"], a["maxq"], a["Hq"], a["Hkv"], a["D"], a["B"],
+                                       a["N"], a["scale"], None)
+
+
+def test_chunked_validation(lib):
+    assert chunked(lib, q=None) == NULL
+    assert chunked(lib, qs=None) == NULL
+    assert chunked(lib, dt=F32) == DTYPE
+    assert chunked(lib, out_dt=7) == DTYPE
+    assert chunked(lib, D=96) == SHAPE
+    assert chunked(lib, B=12) == SHAPE
+    assert chunked(lib, B=4) == SHAPE
+    assert chunked(lib, Hq=6, Hkv=4) == SHAPE
+    assert chunked(lib, Hq=256, Hkv=1) == SHAPE          # group above 128
+    assert chunked(lib, S=-1) == RANGE
+    assert chunked(lib, maxq=65) == RANGE                 # more rows than the batch holds
+    assert chunked(lib, q=fake(1) + 8) == ALIGN
+    assert chunked(lib, out=fake(0) + 8) == ALIGN         # rows are stored 16 bytes at a time
+    assert chunked(lib, qs=fake(6) + 2) == ALIGN
+    assert chunked(lib, k=fake(2), v=fake(2)) == ALIAS
+    assert chunked(lib, out=fake(1)) == ALIAS
+    assert chunked(lib, out=fake(6)) == ALIAS             # output over query_start
+    assert chunked(lib, T=0, maxq=0) == OK                # nothing to do: no CUDA call
+    assert chunked(lib, S=0) == OK
+
+
 def test_write_validation(lib):
     f = lib.paged_kv_write
     assert f(None, fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 128, BF16, None) == NULL

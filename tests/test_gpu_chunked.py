@@ -1,0 +1,97 @@
+"""Multi-query (chunked prefill + decode) paged attention on the GPU against
+the oracle: the chunk's K/V rows written through paged_kv_write, then
+paged_attention_chunked, every output row compared (fp32 output within 2e-3;
+16-bit outputs within max(2e-3, 1 ulp) of the rounded oracle) and the pool
+compared bit-exactly."""
+import math
+
+import pytest
+import torch
+
+import oracle.paged_ops as ops
+from paged_kv_cache_117_gb300 import workloads as wl
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+ATOL = 2e-3
+
+
+def _w(Hq, Hkv, D, B, dtype=torch.bfloat16, N=400, seed=500):
+    return wl.Workload("chunk_case", 0, Hq, Hkv, D, B, N, dtype, 0, seed, "fixed", ())
+
+
+def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None):
+    import paged_kv_cache_117_gb300 as pkv
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    step = gh.plan_chunked(w, prior, counts, width)
+    T = step.query_start[-1]
+    k, v = wl.make_pool(w, "cpu")
+    if poison:   # slots no sequence owns hold NaN: never read, never allowed to leak
+        for b, o in gh.unused_slots(step):
+            k[b, o] = float("nan")
+            v[b, o] = float("nan")
+    g = torch.Generator().manual_seed(w.seed + 77)
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g).to(w.dtype)
+    key, val = wl.make_rows(w, 0, T)
+    kd, vd = k.cuda(), v.cuda()
+    ops.write_kv(k, v, key, val, step.slots)
+    ref = ops.attend_chunked(q, k, v, step.tables, step.lens, step.query_start, w.scale)
+    pkv.paged_kv_write(key.cuda(), val.cuda(), kd, vd,
+                       torch.tensor(step.slots, dtype=torch.int64, device="cuda"))
+    out = torch.full((T, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype, device="cuda")
+    pkv.paged_attention_chunked(out, q.cuda(), kd, vd, wl.pad_tables(step.tables, step.width).cuda(),
+                                torch.tensor(step.lens, dtype=torch.int32, device="cuda"),
+                                torch.tensor(step.query_start, dtype=torch.int32, device="cuda"),
+                                w.scale, max_query_len=max(counts))
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) == 0
+    assert torch.equal(kd.cpu().view(torch.int16), k.view(torch.int16))
+    assert torch.equal(vd.cpu().view(torch.int16), v.view(torch.int16))
+    return gh.assert_close_to_oracle(out, ref, ATOL), step
+
+
+def test_one_prompt_whole():
+    # a fresh prompt in one chunk: 300 tokens, Llama-shaped group of 4
+    _run(_w(8, 2, 128, 16), [0], [300])
+
+
+def test_mixed_batch_prefill_and_decode():
+    # prompt chunks at various offsets, decode tokens, an idle sequence
+    _run(_w(8, 2, 128, 16), [0, 200, 511, 37, 1000, 64, 5],
+         [130, 129, 1, 1, 256, 0, 3])
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 1), (16, 1), (10, 2), (12, 4), (64, 1), (128, 1)])
+def test_group_sizes(hq, hkv):
+    # G = 1, 8, 16, 5 (rows 125 of 128), 3, 64 and 128 (one token per tile)
+    _run(_w(hq, hkv, 64, 16, N=300), [0, 150, 9], [97, 40, 2])
+
+
+@pytest.mark.parametrize("b", [8, 16, 32])
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_and_head_dim(b, d):
+    _run(_w(8, 2, d, b, N=600), [0, 129, 300], [200, 127, 33])
+
+
+def test_f16_cache_and_16bit_outputs():
+    w = _w(8, 2, 128, 16, dtype=torch.float16)
+    _run(w, [0, 90], [150, 70], out_dtype=torch.float16)
+    _run(_w(8, 2, 128, 16), [0, 90], [150, 70], out_dtype=torch.bfloat16)
+
+
+def test_tile_boundaries():
+    # chunk and context lengths on and next to the 128-token tile edges
+    _run(_w(8, 2, 128, 16, N=700), [0, 0, 128, 127, 255, 1, 0],
+         [128, 256, 128, 1, 129, 127, 129])
+
+
+def test_poisoned_unused_slots():
+    # slots past each sequence's length hold NaN in the pool
+    _run(_w(8, 2, 128, 16), [0, 45, 300], [77, 130, 12], poison=True)
+    _run(_w(8, 2, 64, 32), [0, 5], [33, 100], poison=True)
+
+
+def test_wide_table_and_long_context():
+    # table rows wider than needed; one sequence with 3,000 tokens of context
+    _run(_w(8, 2, 128, 16, N=800), [2900, 0], [100, 50], width=300)
