@@ -35,7 +35,7 @@ METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 UNIT = "GB/s"
 FLUSH_BYTES = 256 << 20
 TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
-                      "shared": 2048, "beam": 2048}
+                      "shared": 2048, "beam": 2048, "prefill": 8192}
 SHARING = ("shared", "beam")   # workloads whose sequences share blocks
 
 
@@ -119,6 +119,34 @@ def build_beam_step(w):
     width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
     pairs, slots = hist.pop()
     return list(lens), [list(t) for t in tables], width, slots, pairs, hist
+
+
+def build_chunked_step(w):
+    """Chunked-prefill state built by the library's block manager: every
+    sequence's earlier chunks, then this step's chunk.  Returns lens, tables,
+    width, the chunk rows' slots, the per-sequence query counts and
+    query_start."""
+    import paged_kv_cache_117_gb300 as pkv
+    prior, counts = wl.chunk_plan(w)
+    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    for s, c0 in enumerate(prior):
+        bm.add_sequence(s)
+        if c0:
+            bm.append_tokens(s, c0)
+    slots = torch.cat([bm.append_tokens(s, n)[0] for s, n in enumerate(counts)])
+    tables, lens = zip(*(bm.table(s) for s in range(len(prior))))
+    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    qs = [0]
+    for n in counts:
+        qs.append(qs[-1] + n)
+    return list(lens), [list(t) for t in tables], width, slots, counts, qs
+
+
+def chunked_flops(w, lens, counts):
+    """Multiply-adds x 2 of QK^T and PV over the visible (causal) pairs: query
+    i of a chunk of n in a sequence of L tokens sees L - n + i + 1 keys."""
+    pairs = sum(n * (L - n) + n * (n + 1) // 2 for L, n in zip(lens, counts))
+    return 4 * w.head_dim * w.num_q_heads * pairs
 
 
 def replay_beam_history(w, k, v, hist, dev):
@@ -534,6 +562,183 @@ def run_native(a, world, rank, local):
     return res
 
 
+CHUNK_METRIC = "paged chunked-prefill attn: achieved TFLOP/s (% of GB300 bf16 dense peak)"
+
+
+def peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def chunked_desc(w, width, prior, counts):
+    chunk, mx = w.lens_args
+    return (f"{w.name}: {w.num_seqs} prompt chunks of {chunk} tokens after 0..{mx} cached "
+            f"chunks each (seeded; cached tokens {min(prior)}..{max(prior)}), "
+            f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+            f"{str(w.dtype).replace('torch.', '')}, block {w.block_size}, {w.num_blocks}-block "
+            f"pool, blocks scattered by a seeded permutation, table width {width}, "
+            f"causal within each chunk, q/K/V ~ N(0,1)")
+
+
+def oracle_chunk_sample(w, lens, tables, counts, qs, kc, vc, ids, q, key, value, slots, seq):
+    """fp64 oracle: one sequence's chunk written and attended, on a compact CPU
+    pool holding the blocks ``ids``.  Returns (seconds, FLOPs, threads)."""
+    import oracle.paged_ops as ops
+    remap = {b: i for i, b in enumerate(ids)}
+    B = w.block_size
+    r0, r1 = qs[seq], qs[seq + 1]
+    loc = [remap[int(x) // B] * B + int(x) % B for x in slots[r0:r1]]
+    kc, vc = kc.clone(), vc.clone()
+    t0 = time.perf_counter()
+    ops.write_kv(kc, vc, key[r0:r1], value[r0:r1], loc)
+    ops.attend_chunked(q[r0:r1], kc, vc, [[remap[b] for b in tables[seq]]], [lens[seq]],
+                       [0, r1 - r0], w.scale)
+    dt = time.perf_counter() - t0
+    return dt, chunked_flops(w, [lens[seq]], [counts[seq]]), torch.get_num_threads()
+
+
+def run_native_chunked(a, world, rank, local):
+    import paged_kv_cache_117_gb300 as pkv
+    from paged_kv_cache_117_gb300 import build as pbuild
+    if rank == 0:
+        pbuild.build()
+    barrier(world)
+    pkv.load()
+    assert torch.cuda.is_available(), "the native benchmark needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[a.workload]
+    prior, _ = wl.chunk_plan(w)
+    lens, tables, width, slots_cpu, counts, qs = build_chunked_step(w)
+    T = qs[-1]
+    k, v = wl.make_pool_chunked(w, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 3000)
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g, device=dev).to(w.dtype)
+    key, value = wl.make_rows(w, 0, T, dev)
+    tab_cpu = wl.pad_tables(tables, width)
+    lens_cpu = torch.tensor(lens, dtype=torch.int32)
+    qs_cpu = torch.tensor(qs, dtype=torch.int32)
+    tab, lens_t, qs_t, slots = (x.to(dev) for x in (tab_cpu, lens_cpu, qs_cpu, slots_cpu))
+    maxq = max(counts)
+    out = torch.empty((T, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flops = chunked_flops(w, lens, counts)
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        ids = sorted(set(tables[0]))
+        idx = torch.tensor(ids, device=dev)
+        dt, fl, threads = oracle_chunk_sample(w, lens, tables, counts, qs, k[idx].cpu(),
+                                              v[idx].cpu(), ids, q.cpu(), key.cpu(),
+                                              value.cpu(), slots_cpu.tolist(), 0)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle (torch CPU ops) write + chunked attention of sequence 0 "
+                         f"({counts[0]} queries over {lens[0]} tokens), {dt:.1f} s"}
+
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(d0=None, d1=None):
+        pkv.paged_kv_write(key, value, k, v, slots)
+        if d0 is not None:
+            d0.record(stream)
+        pkv.paged_attention_chunked(out, q, k, v, tab, lens_t, qs_t, w.scale, max_query_len=maxq)
+        if d1 is not None:
+            d1.record(stream)
+
+    for _ in range(max(3, a.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) == 0
+    K = a.steps
+    evs = [(ev(), ev(), ev(), ev()) for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s0, s1, d0, d1 in evs:
+        flush.zero_()
+        s0.record(stream)
+        step(d0, d1)
+        s1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    step_ms = max_over_ranks(world, sum(s0.elapsed_time(s1) for s0, s1, _, _ in evs) / K, dev)
+    dec_ms = max_over_ranks(world, sum(d0.elapsed_time(d1) for _, _, d0, d1 in evs) / K, dev)
+
+    # end to end: q, the chunk's K/V rows, tables, lengths, query_start and
+    # slots in one pinned host buffer -> one H2D copy; the output back in one
+    parts_cpu = [q.cpu(), key.cpu(), value.cpu(), tab_cpu, lens_cpu, qs_cpu, slots_cpu]
+    sizes = [t.numel() * t.element_size() for t in parts_cpu]
+    offs = [0]
+    for n in sizes:
+        offs.append(offs[-1] + (n + 255) // 256 * 256)
+    h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
+    for t, o, n in zip(parts_cpu, offs, sizes):
+        h_in[o:o + n].copy_(t.contiguous().view(torch.uint8).view(-1))
+    e_q, e_key, e_val, e_tab, e_lens, e_qs, e_slots = (
+        d_in[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts_cpu, offs, sizes))
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
+        pkv.paged_attention_chunked(out, e_q, k, v, e_tab, e_lens, e_qs, w.scale,
+                                    max_query_len=maxq)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_evs = [(ev(), ev()) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for e0, e1 in e2e_evs:
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / K, dev)
+    assert pkv.read_device_flags(clear=True) == 0
+
+    peak, kind = peak_bf16()
+    achieved = flops / (dec_ms * 1e-3) / 1e12
+    value_tf = world * flops / (step_ms * 1e-3) / 1e12
+    return {
+        "metric": CHUNK_METRIC, "value": round(value_tf, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": chunked_desc(w, width, prior, counts), "out_dtype": "bfloat16",
+                   "l2": "flushed before every step (256 MiB write, outside the timed span)",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "tokens_per_s": round(world * T / (step_ms * 1e-3), 1),
+        "attention_ms": round(dec_ms, 4),
+        "flops_per_step": flops,
+        "roofline": {"kernel": "paged_attention_chunked (tcgen05)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{kind} bf16_tflops (burst)", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": sum(sizes),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size()},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 4),
+        "cpu_baseline": cpu,
+    }
+
+
 def run_reference(a, world, rank, local):
     """The fp64 CPU oracle as it stands, one bounded sample per step."""
     if rank != 0:
@@ -581,13 +786,52 @@ def run_reference(a, world, rank, local):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_reference_chunked(a, world, rank, local):
+    """The fp64 CPU oracle on the chunked workload: one sequence's chunk per
+    step (the shortest one, to bound the time)."""
+    if rank != 0:
+        return None
+    w = wl.WORKLOADS[a.workload]
+    prior, _ = wl.chunk_plan(w)
+    lens, tables, width, slots, counts, qs = build_chunked_step(w)
+    seq = min(range(len(lens)), key=lambda s: lens[s])
+    ids = sorted(set(tables[seq]))
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    shape = (len(ids), w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.randn(shape, generator=g).to(w.dtype)
+    vc = torch.randn(shape, generator=g).to(w.dtype)
+    T = qs[-1]
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g).to(w.dtype)
+    key, value = wl.make_rows(w, 0, T)
+    times, fl, threads = [], 0, torch.get_num_threads()
+    for i in range(max(3, a.warmup) + a.steps):
+        dt, fl, threads = oracle_chunk_sample(w, lens, tables, counts, qs, kc, vc, ids, q, key,
+                                              value, slots.tolist(), seq)
+        if i >= max(3, a.warmup):
+            times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    val = fl / (ms * 1e-3) / 1e12
+    sample = (f"fp64 oracle write + chunked attention of sequence {seq} per step "
+              f"({counts[seq]} queries over {lens[seq]} tokens)")
+    return {"impl": "reference", "metric": CHUNK_METRIC, "value": round(val, 6),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": chunked_desc(w, width, prior, counts)},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main():
     a = parse_args()
     world, rank, local = dist_init()
+    chunked = wl.WORKLOADS[a.workload].lens_kind == "chunked"
     if a.impl == "reference":
-        res = run_reference(a, world, rank, local)
+        res = (run_reference_chunked if chunked else run_reference)(a, world, rank, local)
     else:
-        res = run_native(a, world, rank, local)
+        res = (run_native_chunked if chunked else run_native)(a, world, rank, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

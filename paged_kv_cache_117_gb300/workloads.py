@@ -24,6 +24,9 @@ The five workloads follow the shapes the pages use for their examples:
                   vLLM ...", Step 4): 16 prompts of 1,000 tokens, 8 samples each.
 * ``beam``     -- beam search over shared prompts (same Step 4): 32 prompts of
                   1,000 tokens, 8 beams each, seeded scores in place of a model.
+* ``prefill``  -- chunked prefill ("Paging the KV Cache Like an OS", continuous
+                  batching): 16 prompt chunks of 512 tokens after 0..15 cached
+                  chunks each.
 
 The pages measure on ShareGPT/Alpaca traces; none is used or reproduced here.
 Lengths come from the seeded distributions below instead.
@@ -49,7 +52,7 @@ class Workload:
     dtype: torch.dtype
     partition_tokens: int          # 0 = one partition per sequence
     seed: int
-    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam"
+    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam" | "chunked"
     lens_args: tuple = field(default_factory=tuple)
 
     @property
@@ -86,7 +89,14 @@ SHARED = Workload("shared", 128, 32, 8, 128, 16, 4_096, torch.bfloat16, 512, 122
 BEAM = Workload("beam", 256, 32, 8, 128, 16, 8_192, torch.bfloat16, 512, 123,
                 "beam", (32, 1000, 8, 2, 20))
 
-WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM)}
+# Chunked prefill ("Paging the KV Cache Like an OS", continuous batching): a
+# step's budget of 8,192 tokens filled with 512-token prompt chunks of 16
+# sequences, each of which already holds 0..15 earlier chunks of its prompt
+# (seeded), Llama-3.1-8B heads.
+PREFILL = Workload("prefill", 16, 32, 8, 128, 16, 16_384, torch.bfloat16, 0, 124,
+                   "chunked", (512, 15))
+
+WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM, PREFILL)}
 
 
 def scaled(w: Workload, num_seqs: int, max_len: Optional[int] = None,
@@ -222,6 +232,15 @@ def scatter_block_tables(lens: Sequence[int], block_size: int,
         tables.append([int(b) for b in order[pos:pos + nb]])
         pos += nb
     return tables
+
+
+def chunk_plan(w: Workload):
+    """(prior tokens, this step's query tokens) per sequence of a chunked
+    prefill workload."""
+    chunk, max_prior = w.lens_args
+    g = _gen(w.seed)
+    prior = (torch.randint(0, max_prior + 1, (w.num_seqs,), generator=g) * chunk).tolist()
+    return [int(x) for x in prior], [chunk] * w.num_seqs
 
 
 @dataclass(frozen=True)

@@ -95,3 +95,54 @@ def test_poisoned_unused_slots():
 def test_wide_table_and_long_context():
     # table rows wider than needed; one sequence with 3,000 tokens of context
     _run(_w(8, 2, 128, 16, N=800), [2900, 0], [100, 50], width=300)
+
+
+def test_prefill_full_size_sampled():
+    """The benchmark's prefill workload at full size, in its launch
+    configuration (16 chunks of 512 tokens after up to 7,168 cached tokens,
+    512-block table rows, bf16 output): the chunk's writes bit-exact on the
+    sampled sequences' blocks, and sampled rows against the oracle (a row at
+    position p is decode attention over positions 0..p)."""
+    import random
+    import paged_kv_cache_117_gb300 as pkv
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = wl.PREFILL
+    prior, counts = wl.chunk_plan(w)
+    step = gh.plan_chunked(w, prior, counts, width=8192 // w.block_size)
+    T = step.query_start[-1]
+    k, v = wl.make_pool_chunked(w, "cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed + 3000)
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g, device="cuda").to(w.dtype)
+    key, val = wl.make_rows(w, 0, T, "cuda")
+    lens = step.lens
+    seqs = sorted({0, max(range(len(lens)), key=lambda s: lens[s]),
+                   min(range(len(lens)), key=lambda s: lens[s])})
+    ids = sorted({b for s in seqs for b in step.tables[s]})
+    remap = {b: i for i, b in enumerate(ids)}
+    idx = torch.tensor(ids, device="cuda")
+    kb, vb = k[idx].cpu(), v[idx].cpu()
+    B = w.block_size
+    rows = [r for s in seqs for r in range(step.query_start[s], step.query_start[s + 1])]
+    ops.write_kv(kb, vb, key.cpu()[rows], val.cpu()[rows],
+                 [remap[step.slots[r] // B] * B + step.slots[r] % B for r in rows])
+    out = torch.empty((T, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    pkv.paged_kv_write(key, val, k, v, torch.tensor(step.slots, dtype=torch.int64, device="cuda"))
+    pkv.paged_attention_chunked(out, q, k, v, wl.pad_tables(step.tables, step.width).cuda(),
+                                torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                torch.tensor(step.query_start, dtype=torch.int32, device="cuda"),
+                                w.scale, max_query_len=max(counts))
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) == 0
+    assert torch.equal(k[idx].cpu(), kb) and torch.equal(v[idx].cpu(), vb)
+    assert torch.isfinite(out).all()
+    rnd = random.Random(3)
+    qc = q.cpu()
+    for s in seqs:
+        n, L, r0 = counts[s], lens[s], step.query_start[s]
+        for i in sorted({0, 1, 31, 32, 127, 128, n // 2, n - 1, rnd.randrange(n)}):
+            p = L - n + i
+            ref = ops.attend(qc[r0 + i:r0 + i + 1], kb, vb, [[remap[b] for b in step.tables[s]]],
+                             [p + 1], w.scale)
+            gh.assert_close_to_oracle(out[r0 + i:r0 + i + 1], ref, ATOL)
