@@ -202,7 +202,7 @@ pkv_status paged_attention_decode(
  * skipped (its rows are left untouched) and flagged PKV_FLAG_LEN_RANGE; L_s
  * past the table is clamped and flagged; bad block ids are read as zeros and
  * flagged PKV_FLAG_BLOCK_RANGE.  No workspace: one launch, one CTA per
- * (query tile of 128 / G tokens, sequence, KV head).
+ * (two query tiles of 128 / G tokens each, sequence, KV head).
  */
 pkv_status paged_attention_chunked(
     void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,

@@ -381,6 +381,7 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
   p.group = group;
   p.tile_tokens = tile_tokens;
   p.num_qtiles = (int)qtiles;
+  p.num_qpairs = (int)((qtiles + 1) / 2);
   p.max_query_len = max_query_len;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -77,7 +77,7 @@ cudaError_t launch_decode_f16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeParams &p, int head_dim, int block_size,
                               cudaStream_t stream, int *launches);
 
-// Multi-query (chunked prefill) attention: one CTA per (query tile,
+// Multi-query (chunked prefill) attention: one CTA per (pair of query tiles,
 // sequence, KV head).  A query tile is tile_tokens = 128 / group tokens.
 struct ChunkedParams {
   void *out;                     // [num_tokens, Hq, D]
@@ -93,6 +93,7 @@ struct ChunkedParams {
   int group;
   int tile_tokens;
   int num_qtiles;                // ceil(max_query_len / tile_tokens)
+  int num_qpairs;                // ceil(num_qtiles / 2): query tiles go two to a CTA
   int max_query_len;
   int num_blocks;
   float scale_log2;
