@@ -202,19 +202,32 @@ DECODE_SOURCES = ("paged_kv_cache_117_gb300/csrc/decode_kernel.cuh",
                   "paged_kv_cache_117_gb300/csrc/capi.cu")
 
 
-def measured_traffic(workload, partition_tokens):
-    """DRAM bytes per attention launch from the committed ncu summary, or None
-    when it was taken on another workload or the decode sources changed since."""
+CHUNKED_SOURCES = ("paged_kv_cache_117_gb300/csrc/chunked_kernel.cuh",
+                   "paged_kv_cache_117_gb300/csrc/pkv_device.cuh",
+                   "paged_kv_cache_117_gb300/csrc/pkv_tcgen05.cuh",
+                   "paged_kv_cache_117_gb300/csrc/pkv_launch.h",
+                   "paged_kv_cache_117_gb300/csrc/capi.cu")
+
+
+def sources_sha256(sources):
     import hashlib
+    h = hashlib.sha256()
+    for f in sources:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, partition_tokens, profile="decode_kernel_llama8b.md",
+                     sources=DECODE_SOURCES):
+    """DRAM bytes per launch from a committed ncu summary, or None when it was
+    taken on another workload or the kernel's sources changed since."""
     try:
-        text = open(os.path.join(ROOT, "profiles", "decode_kernel_llama8b.md")).read()
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
         kv = dict(line.split(": ", 1) for line in text.splitlines()
                   if line.startswith(("traffic_", "source_sha256")))
-        h = hashlib.sha256()
-        for f in DECODE_SOURCES:
-            with open(os.path.join(ROOT, f), "rb") as fh:
-                h.update(fh.read())
-        if (kv.get("source_sha256") == h.hexdigest() and kv.get("traffic_workload") == workload
+        if (kv.get("source_sha256") == sources_sha256(sources)
+                and kv.get("traffic_workload") == workload
                 and int(kv.get("traffic_partition_tokens", -1)) == partition_tokens):
             return int(kv["traffic_bytes_per_launch"])
     except Exception:
@@ -728,7 +741,9 @@ def run_native_chunked(a, world, rank, local):
         "roofline": {"kernel": "paged_attention_chunked (tcgen05)", "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{kind} bf16_tflops (burst)", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4),
+                     "traffic": measured_traffic(w.name, 0, "chunked_kernel_prefill.md",
+                                                 CHUNKED_SOURCES)},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": sum(sizes),
                 "d2h_bytes_per_step": h_out.numel() * h_out.element_size()},
