@@ -20,6 +20,10 @@ Contents, each written from the pages' description:
   (``attend_chunked``: each query attends causally to its own sequence's
   positions up to its own; "Paging the KV Cache Like an OS", continuous
   batching and chunked prefill).
+* ``prefix_cache`` -- block pool with a prefix cache: chained SHA-256 block
+  keys, a hash -> block map of full blocks, a free queue whose order is the
+  eviction order ("PagedAttention and vLLM ...", section 2.4 and summary
+  point 5).
 * ``sizing`` -- KV bytes per token and per block ("PagedAttention: Virtual
   Memory for the KV Cache", memory-bound section; "Batching and
   PagedAttention", bytes-per-block formula).
