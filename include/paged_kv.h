@@ -334,6 +334,82 @@ pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear,
  */
 const char *pkv_last_error_string(void);
 
+/*
+ * Host-side block manager with a prefix cache (no device memory involved).
+ *
+ * "PagedAttention and vLLM: Paging the KV Cache Like an OS" ..., section 2.4
+ * (V1's block pool and hash chain) and summary point 5: full blocks are keyed
+ * by a chained hash and stay in a key -> block map after their request
+ * finishes, so that a later request whose prompt starts the same way takes
+ * them over and skips their prefill.
+ *  - Key of a full block: SHA-256 of the message (parent key: 32 bytes; each
+ *    of the block's block_size token ids: 4 bytes little-endian; extra key:
+ *    8 bytes little-endian).  The first block's parent key is 32 zero bytes.
+ *    The extra key separates caches that must not mix (e.g. adapters).
+ *  - Free blocks wait in one queue ordered by recency of release: a finished
+ *    request's blocks go to the back (its last block first), allocation takes
+ *    the front, and a block taken from the front leaves the map if it was
+ *    cached.  The queue order is the eviction order.
+ *  - Cached blocks are full and never written again: each request fills its
+ *    own last block, so nothing is ever copied on write.
+ * Not thread-safe: one manager, one thread at a time.
+ */
+typedef struct pkv_prefix_cache pkv_prefix_cache;
+
+/* A manager of num_blocks blocks of block_size tokens; free_order (NULL =
+ * ascending) is the initial queue, a permutation of 0..num_blocks-1.  Returns
+ * NULL on invalid arguments.  Release with pkv_pc_destroy. */
+pkv_prefix_cache *pkv_pc_create(int num_blocks, int block_size,
+                                const int32_t *free_order);
+void pkv_pc_destroy(pkv_prefix_cache *pc);
+
+/* New request `seq` with prompt[0..prompt_len): walks the prompt's key chain
+ * over the full blocks inside its first prompt_len - 1 tokens (the last
+ * token is always recomputed) and takes over every block up to the first
+ * miss.  *num_cached_tokens = the prompt tokens already in the cache (a
+ * multiple of block_size); the caller appends the rest with pkv_pc_append.
+ * PKV_ERR_RANGE if seq exists or prompt_len < 0. */
+pkv_status pkv_pc_add_sequence(pkv_prefix_cache *pc, int64_t seq,
+                               const int32_t *prompt, int prompt_len,
+                               uint64_t extra_key, int *num_cached_tokens);
+
+/* Reserves slots for the sequence's next n tokens (their ids in tokens[]):
+ * slots[i] = block * block_size + offset.  A block that becomes full is keyed
+ * and entered in the map unless its key is cached already.  Refuses with
+ * PKV_ERR_NO_BLOCKS, changing nothing, when the call needs more blocks than
+ * the free queue holds. */
+pkv_status pkv_pc_append(pkv_prefix_cache *pc, int64_t seq,
+                         const int32_t *tokens, int n, int64_t *slots);
+
+/* Finishes the request: every block's count drops; blocks reaching zero go
+ * to the back of the free queue, keeping their cached keys. */
+pkv_status pkv_pc_free_sequence(pkv_prefix_cache *pc, int64_t seq);
+
+/* The sequence's block table (up to capacity entries), its block and token
+ * counts. */
+pkv_status pkv_pc_table(const pkv_prefix_cache *pc, int64_t seq, int32_t *out,
+                        int capacity, int *num_blocks, int64_t *num_tokens);
+
+/* Blocks in the free queue (cached ones included); entries in the map. */
+int pkv_pc_num_free(const pkv_prefix_cache *pc);
+int pkv_pc_num_cached(const pkv_prefix_cache *pc);
+/* Reference count of a block (-1 if out of range). */
+int pkv_pc_refcount(const pkv_prefix_cache *pc, int block);
+/* *cached = 1 and key32[0..32) = the block's key when the block is cached. */
+pkv_status pkv_pc_block_key(const pkv_prefix_cache *pc, int block,
+                            uint8_t *key32, int *cached);
+/* The free queue from front to back (up to capacity entries); *count = its
+ * length. */
+pkv_status pkv_pc_free_queue(const pkv_prefix_cache *pc, int32_t *out,
+                             int capacity, int *count);
+/* Keys of the num_tokens / block_size full blocks of a token stream (32
+ * bytes each, in order) -- the chain a request would look up. */
+pkv_status pkv_pc_chain_keys(const int32_t *tokens, int num_tokens,
+                             int block_size, uint64_t extra_key,
+                             uint8_t *keys_out);
+/* SHA-256 (FIPS 180-4) of msg[0..len) into digest32[0..32). */
+pkv_status pkv_sha256(const void *msg, size_t len, uint8_t *digest32);
+
 #ifdef __cplusplus
 }
 #endif

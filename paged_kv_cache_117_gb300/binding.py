@@ -35,6 +35,11 @@ EXPORTED_SYMBOLS = (
     "pkv_last_error_string",
     "paged_attention_decode_noalloc",
     "paged_attention_chunked",
+    "pkv_pc_create",
+    "pkv_pc_add_sequence",
+    "pkv_pc_append",
+    "pkv_pc_free_sequence",
+    "pkv_sha256",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence", "pkv_bm_fork",
     "pkv_bm_free_sequence", "pkv_bm_append", "pkv_bm_table", "pkv_bm_num_free",
     "pkv_bm_refcount",
@@ -106,6 +111,33 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_bm_num_free.restype = ci
     lib.pkv_bm_refcount.argtypes = [vp, ci]
     lib.pkv_bm_refcount.restype = ci
+    u64, u8p = ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint8)
+    lib.pkv_pc_create.argtypes = [ci, ci, vp]
+    lib.pkv_pc_create.restype = vp
+    lib.pkv_pc_destroy.argtypes = [vp]
+    lib.pkv_pc_destroy.restype = None
+    lib.pkv_pc_add_sequence.argtypes = [vp, i64, vp, ci, u64, ctypes.POINTER(ci)]
+    lib.pkv_pc_add_sequence.restype = ci
+    lib.pkv_pc_append.argtypes = [vp, i64, vp, ci, vp]
+    lib.pkv_pc_append.restype = ci
+    lib.pkv_pc_free_sequence.argtypes = [vp, i64]
+    lib.pkv_pc_free_sequence.restype = ci
+    lib.pkv_pc_table.argtypes = [vp, i64, vp, ci, ctypes.POINTER(ci), i64p]
+    lib.pkv_pc_table.restype = ci
+    lib.pkv_pc_num_free.argtypes = [vp]
+    lib.pkv_pc_num_free.restype = ci
+    lib.pkv_pc_num_cached.argtypes = [vp]
+    lib.pkv_pc_num_cached.restype = ci
+    lib.pkv_pc_refcount.argtypes = [vp, ci]
+    lib.pkv_pc_refcount.restype = ci
+    lib.pkv_pc_block_key.argtypes = [vp, ci, vp, ctypes.POINTER(ci)]
+    lib.pkv_pc_block_key.restype = ci
+    lib.pkv_pc_free_queue.argtypes = [vp, vp, ci, ctypes.POINTER(ci)]
+    lib.pkv_pc_free_queue.restype = ci
+    lib.pkv_pc_chain_keys.argtypes = [vp, ci, ci, u64, vp]
+    lib.pkv_pc_chain_keys.restype = ci
+    lib.pkv_sha256.argtypes = [vp, ctypes.c_size_t, vp]
+    lib.pkv_sha256.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -339,3 +371,106 @@ class BlockManager:
 
     def refcount(self, block: int) -> int:
         return int(self._lib.pkv_bm_refcount(self._h, int(block)))
+
+
+def _i32(xs) -> torch.Tensor:
+    return torch.as_tensor(list(xs), dtype=torch.int32).contiguous()
+
+
+def sha256(data: bytes) -> bytes:
+    """SHA-256 digest computed by the library."""
+    buf = ctypes.create_string_buffer(bytes(data), max(1, len(data)))
+    out = (ctypes.c_uint8 * 32)()
+    _check("pkv_sha256", load().pkv_sha256(ctypes.cast(buf, ctypes.c_void_p), len(data),
+                                           ctypes.cast(out, ctypes.c_void_p)))
+    return bytes(out)
+
+
+def chain_keys(tokens, block_size: int, extra_key: int = 0):
+    """Chained keys (32 bytes each) of every full block of a token stream."""
+    t = _i32(tokens)
+    nb = t.numel() // int(block_size)
+    out = (ctypes.c_uint8 * max(1, 32 * nb))()
+    _check("pkv_pc_chain_keys", load().pkv_pc_chain_keys(
+        t.data_ptr() if t.numel() else None, t.numel(), int(block_size), int(extra_key),
+        ctypes.cast(out, ctypes.c_void_p)))
+    raw = bytes(out)
+    return [raw[32 * i:32 * (i + 1)] for i in range(nb)]
+
+
+class PrefixCache:
+    """The library's block manager with a prefix cache (pkv_pc_* in the C
+    ABI): chained block keys, a key -> block map of full blocks, and a free
+    queue whose order is the eviction order."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self._lib = load()
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        order = None if free_order is None else _i32(free_order)
+        if order is not None and order.numel() != num_blocks:
+            raise ValueError("free_order must list every block once")
+        self._order = order
+        h = self._lib.pkv_pc_create(int(num_blocks), int(block_size),
+                                    None if order is None else order.data_ptr())
+        if not h:
+            raise ValueError("invalid prefix cache arguments")
+        self._h = h
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pkv_pc_destroy(h)
+
+    def add_sequence(self, seq: int, prompt, extra_key: int = 0) -> int:
+        """Start a request; returns the number of prompt tokens already cached."""
+        t = _i32(prompt)
+        n = ctypes.c_int(0)
+        _check("pkv_pc_add_sequence", self._lib.pkv_pc_add_sequence(
+            self._h, int(seq), t.data_ptr() if t.numel() else None, t.numel(), int(extra_key),
+            ctypes.byref(n)))
+        return int(n.value)
+
+    def append(self, seq: int, tokens) -> torch.Tensor:
+        """Slots (int64, CPU) of the sequence's next tokens."""
+        t = _i32(tokens)
+        slots = torch.empty(max(t.numel(), 1), dtype=torch.int64)
+        _check("pkv_pc_append", self._lib.pkv_pc_append(
+            self._h, int(seq), t.data_ptr() if t.numel() else None, t.numel(), slots.data_ptr()))
+        return slots[: t.numel()]
+
+    def free_sequence(self, seq: int) -> None:
+        _check("pkv_pc_free_sequence", self._lib.pkv_pc_free_sequence(self._h, int(seq)))
+
+    def table(self, seq: int):
+        nb, nt = ctypes.c_int(0), ctypes.c_int64(0)
+        _check("pkv_pc_table", self._lib.pkv_pc_table(self._h, int(seq), None, 0,
+                                                      ctypes.byref(nb), ctypes.byref(nt)))
+        out = torch.empty(max(nb.value, 1), dtype=torch.int32)
+        _check("pkv_pc_table", self._lib.pkv_pc_table(self._h, int(seq), out.data_ptr(), nb.value,
+                                                      ctypes.byref(nb), ctypes.byref(nt)))
+        return out[: nb.value].tolist(), int(nt.value)
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_pc_num_free(self._h))
+
+    def num_cached(self) -> int:
+        return int(self._lib.pkv_pc_num_cached(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_pc_refcount(self._h, int(block)))
+
+    def block_key(self, block: int):
+        """The block's cached key (bytes), or None."""
+        out = (ctypes.c_uint8 * 32)()
+        cached = ctypes.c_int(0)
+        _check("pkv_pc_block_key", self._lib.pkv_pc_block_key(
+            self._h, int(block), ctypes.cast(out, ctypes.c_void_p), ctypes.byref(cached)))
+        return bytes(out) if cached.value else None
+
+    def free_queue(self):
+        """The free queue from front (next to allocate / evict) to back."""
+        out = torch.empty(max(self.num_blocks, 1), dtype=torch.int32)
+        n = ctypes.c_int(0)
+        _check("pkv_pc_free_queue", self._lib.pkv_pc_free_queue(
+            self._h, out.data_ptr(), self.num_blocks, ctypes.byref(n)))
+        return out[: n.value].tolist()
