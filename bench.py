@@ -35,7 +35,7 @@ METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 UNIT = "GB/s"
 FLUSH_BYTES = 256 << 20
 TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
-                      "shared": 2048, "beam": 2048, "prefill": 8192}
+                      "shared": 2048, "beam": 2048, "prefill": 8192, "prefix": 4096}
 SHARING = ("shared", "beam")   # workloads whose sequences share blocks
 
 
@@ -140,6 +140,54 @@ def build_chunked_step(w):
     for n in counts:
         qs.append(qs[-1] + n)
     return list(lens), [list(t) for t in tables], width, slots, counts, qs
+
+
+def build_prefix_step(w):
+    """Prefix-caching state built by the library's prefix-cache manager: one
+    earlier request per system prompt prefilled it (its full blocks stay
+    cached after it finished), then every request looks its prompt up and
+    prefills only the rest.  Returns lens, tables, width, slots, counts,
+    query_start and the prompt tokens the cache saved."""
+    import paged_kv_cache_117_gb300 as pkv
+    plan = wl.prefix_plan(w)
+    pc = pkv.PrefixCache(w.num_blocks, w.block_size, wl.free_block_order(w))
+    for i, sysp in enumerate(plan.systems):
+        sid = len(plan.prompts) + i
+        warm = sysp + [0]
+        c = pc.add_sequence(sid, warm)
+        pc.append(sid, warm[c:])
+        pc.free_sequence(sid)
+    slots, counts, saved = [], [], 0
+    for r, prompt in enumerate(plan.prompts):
+        c = pc.add_sequence(r, prompt)
+        slots.append(pc.append(r, prompt[c:]))
+        counts.append(len(prompt) - c)
+        saved += c
+    tables, lens = zip(*(pc.table(r) for r in range(len(plan.prompts))))
+    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    qs = [0]
+    for n in counts:
+        qs.append(qs[-1] + n)
+    return list(lens), [list(t) for t in tables], width, torch.cat(slots), counts, qs, saved
+
+
+def build_multiquery_step(w):
+    """(lens, tables, width, slots, counts, query_start, description) of a
+    multi-query workload."""
+    if w.lens_kind == "prefix":
+        lens, tables, width, slots, counts, qs, saved = build_prefix_step(w)
+        n_sys, sys_len, q_len = w.lens_args
+        desc = (f"{w.name}: {w.num_seqs} requests, each one of {n_sys} system prompts of "
+                f"{sys_len} tokens + its own {q_len}-token question (seeded token ids); the system "
+                f"prompts' full blocks are in the prefix cache (chained SHA-256 keys), so "
+                f"{saved} of {saved + sum(counts)} prompt tokens are taken over and each request "
+                f"prefills {counts[0]} tokens attending over {lens[0]}; "
+                f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+                f"{str(w.dtype).replace('torch.', '')}, block {w.block_size}, {w.num_blocks}-block pool")
+        return lens, tables, width, slots, counts, qs, desc
+    prior, _ = wl.chunk_plan(w)
+    lens, tables, width, slots, counts, qs = build_chunked_step(w)
+    return lens, tables, width, slots, counts, qs, chunked_desc(w, width, prior, counts)
 
 
 def chunked_flops(w, lens, counts):
@@ -624,8 +672,7 @@ def run_native_chunked(a, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[a.workload]
-    prior, _ = wl.chunk_plan(w)
-    lens, tables, width, slots_cpu, counts, qs = build_chunked_step(w)
+    lens, tables, width, slots_cpu, counts, qs, desc = build_multiquery_step(w)
     T = qs[-1]
     k, v = wl.make_pool_chunked(w, dev)
     g = torch.Generator(device=dev)
@@ -732,7 +779,7 @@ def run_native_chunked(a, world, rank, local):
         "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": chunked_desc(w, width, prior, counts), "out_dtype": "bfloat16",
+        "config": {"workload": desc, "out_dtype": "bfloat16",
                    "l2": "flushed before every step (256 MiB write, outside the timed span)",
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "tokens_per_s": round(world * T / (step_ms * 1e-3), 1),
@@ -807,8 +854,7 @@ def run_reference_chunked(a, world, rank, local):
     if rank != 0:
         return None
     w = wl.WORKLOADS[a.workload]
-    prior, _ = wl.chunk_plan(w)
-    lens, tables, width, slots, counts, qs = build_chunked_step(w)
+    lens, tables, width, slots, counts, qs, desc = build_multiquery_step(w)
     seq = min(range(len(lens)), key=lambda s: lens[s])
     ids = sorted(set(tables[seq]))
     g = torch.Generator().manual_seed(w.seed + 2000)
@@ -832,7 +878,7 @@ def run_reference_chunked(a, world, rank, local):
             "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": chunked_desc(w, width, prior, counts)},
+            "config": {"workload": desc},
             "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -842,7 +888,7 @@ def run_reference_chunked(a, world, rank, local):
 def main():
     a = parse_args()
     world, rank, local = dist_init()
-    chunked = wl.WORKLOADS[a.workload].lens_kind == "chunked"
+    chunked = wl.WORKLOADS[a.workload].lens_kind in ("chunked", "prefix")
     if a.impl == "reference":
         res = (run_reference_chunked if chunked else run_reference)(a, world, rank, local)
     else:

@@ -27,6 +27,9 @@ The five workloads follow the shapes the pages use for their examples:
 * ``prefill``  -- chunked prefill ("Paging the KV Cache Like an OS", continuous
                   batching): 16 prompt chunks of 512 tokens after 0..15 cached
                   chunks each.
+* ``prefix``   -- prefix caching (same page, section 2.4): 32 requests over 2
+                  cached 2,048-token system prompts, each prefilling its own
+                  256-token question.
 
 The pages measure on ShareGPT/Alpaca traces; none is used or reproduced here.
 Lengths come from the seeded distributions below instead.
@@ -52,7 +55,7 @@ class Workload:
     dtype: torch.dtype
     partition_tokens: int          # 0 = one partition per sequence
     seed: int
-    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam" | "chunked"
+    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam" | "chunked" | "prefix"
     lens_args: tuple = field(default_factory=tuple)
 
     @property
@@ -96,7 +99,15 @@ BEAM = Workload("beam", 256, 32, 8, 128, 16, 8_192, torch.bfloat16, 512, 123,
 PREFILL = Workload("prefill", 16, 32, 8, 128, 16, 16_384, torch.bfloat16, 0, 124,
                    "chunked", (512, 15))
 
-WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM, PREFILL)}
+# Prefix caching ("Paging the KV Cache Like an OS", section 2.4 and summary
+# point 5): 32 requests share one of 2 system prompts of 2,048 tokens and add a
+# 256-token question of their own; the system prompts were prefilled (and
+# their blocks cached) by earlier requests, so each request prefills only its
+# question, attending over 2,304 tokens.  Token ids are seeded.
+PREFIX = Workload("prefix", 32, 32, 8, 128, 16, 16_384, torch.bfloat16, 0, 125,
+                  "prefix", (2, 2048, 256))
+
+WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM, PREFILL, PREFIX)}
 
 
 def scaled(w: Workload, num_seqs: int, max_len: Optional[int] = None,
@@ -241,6 +252,20 @@ def chunk_plan(w: Workload):
     g = _gen(w.seed)
     prior = (torch.randint(0, max_prior + 1, (w.num_seqs,), generator=g) * chunk).tolist()
     return [int(x) for x in prior], [chunk] * w.num_seqs
+
+
+@dataclass(frozen=True)
+class PrefixPlan:
+    systems: List[List[int]]        # token ids of each system prompt
+    prompts: List[List[int]]        # each request's prompt (system + question)
+
+
+def prefix_plan(w: Workload) -> PrefixPlan:
+    n_sys, sys_len, q_len = w.lens_args
+    g = _gen(w.seed)
+    systems = torch.randint(0, 32000, (n_sys, sys_len), generator=g).tolist()
+    questions = torch.randint(0, 32000, (w.num_seqs, q_len), generator=g).tolist()
+    return PrefixPlan(systems, [systems[r % n_sys] + questions[r] for r in range(w.num_seqs)])
 
 
 @dataclass(frozen=True)
