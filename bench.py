@@ -396,6 +396,18 @@ def sample_blocks(tables, nseq):
     return seqs, sorted({b for s in seqs for b in tables[s]})
 
 
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value, slots, seqs):
     """fp64 oracle over ``seqs``: KV write then attention, on a compact CPU
     pool ``kc``/``vc`` holding the blocks ``ids``.  Returns (seconds,
@@ -480,6 +492,7 @@ def run_native(a, world, rank, local):
         dt, b, threads = oracle_sample_time(w, lens, tables, width, k[idx].cpu(), v[idx].cpu(),
                                             ids, q, key, value, slots_cpu.tolist(), seqs)
         cpu = {"value": b / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
                "sample": f"fp64 oracle (torch CPU ops) KV write + attention of the first "
                          f"{min(a.cpu_seqs, w.num_seqs)} of {w.num_seqs} sequences, "
                          f"{dt:.1f} s; bytes = unique K/V rows read + new rows written"}
@@ -607,6 +620,8 @@ def run_native(a, world, rank, local):
         "seq_steps_per_s": round(world * w.num_seqs / (step_ms * 1e-3), 1),
         "attention_ms": round(dec_ms, 4),
         "bytes_per_step": nbytes,
+        **({"unique_kv_gbs": round(world * a.layers * (nbytes["step"] - nbytes["kv"] + nbytes["kv_unique"])
+                                   / (step_ms * 1e-3) / 1e9, 1)} if "kv_unique" in nbytes else {}),
         "roofline": {"kernel": "paged_attention_decode (work list + attention with fused merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
@@ -696,6 +711,7 @@ def run_native_chunked(a, world, rank, local):
                                               v[idx].cpu(), ids, q.cpu(), key.cpu(),
                                               value.cpu(), slots_cpu.tolist(), 0)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
                "sample": f"fp64 oracle (torch CPU ops) write + chunked attention of sequence 0 "
                          f"({counts[0]} queries over {lens[0]} tokens), {dt:.1f} s"}
 
