@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step: one K/V pool per layer, shared block tables")
+    ap.add_argument("--p-format", choices=["hilo", "f16"], default="hilo",
+                    help="chunked workloads: P as hi + lo 16-bit operands, or as one f16 operand")
     ap.add_argument("--graph", action="store_true",
                     help="capture the whole step (all layers) in one CUDA graph and replay it")
     return ap.parse_args()
@@ -722,7 +724,8 @@ def run_native_chunked(a, world, rank, local):
         pkv.paged_kv_write(key, value, k, v, slots)
         if d0 is not None:
             d0.record(stream)
-        pkv.paged_attention_chunked(out, q, k, v, tab, lens_t, qs_t, w.scale, max_query_len=maxq)
+        pkv.paged_attention_chunked(out, q, k, v, tab, lens_t, qs_t, w.scale, max_query_len=maxq,
+                                    p_format=a.p_format)
         if d1 is not None:
             d1.record(stream)
 
@@ -770,7 +773,7 @@ def run_native_chunked(a, world, rank, local):
         d_in.copy_(h_in, non_blocking=True)
         pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
         pkv.paged_attention_chunked(out, e_q, k, v, e_tab, e_lens, e_qs, w.scale,
-                                    max_query_len=maxq)
+                                    max_query_len=maxq, p_format=a.p_format)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -795,7 +798,7 @@ def run_native_chunked(a, world, rank, local):
         "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": desc, "out_dtype": "bfloat16",
+        "config": {"workload": desc, "out_dtype": "bfloat16", "p_format": a.p_format,
                    "l2": "flushed before every step (256 MiB write, outside the timed span)",
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "tokens_per_s": round(world * T / (step_ms * 1e-3), 1),

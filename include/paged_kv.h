@@ -77,6 +77,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 #define PKV_FLAG_PAIR_RANGE 0x4u  /* a copy pair named a block outside the pool */
 #define PKV_FLAG_LEN_RANGE 0x8u   /* a context length was < 0 or > max_blocks * block_size */
 #define PKV_FLAG_TIMEOUT 0x10u    /* a kernel gave up waiting on its own tile loads */
+#define PKV_FLAG_V_RANGE 0x20u    /* PKV_P_F16 met a bf16 V value beyond the f16 range (clamped) */
 
 /*
  * paged_kv_write -- store new keys/values into their slots.
@@ -168,6 +169,21 @@ pkv_status paged_attention_decode(
     int num_blocks, float scale, int partition_tokens, void *workspace,
     size_t workspace_bytes, pkv_stream_t stream);
 
+/* How P (the softmax weights) enters the P.V product of
+ * paged_attention_chunked; scores, the softmax and accumulation are fp32
+ * either way. */
+typedef enum {
+  PKV_P_HILO = 0, /* P = hi + lo, two 16-bit MMA operands of the cache dtype:
+                     about 16 significant bits (errors ~1e-5) */
+  PKV_P_F16 = 1   /* P as one f16 operand (11 significant bits) and V as f16
+                     (a bf16 V tile is converted in shared memory; values
+                     beyond +-65504 are clamped and flagged
+                     PKV_FLAG_V_RANGE); half the P.V tensor work; each
+                     output row is an exact convex combination of the f16
+                     values with the rounded weights, error per element below
+                     2^-11 * max|V - out| */
+} pkv_p_format;
+
 /*
  * paged_attention_chunked -- multi-query attention over the paged context:
  * chunks of prompts (chunked prefill) and decode tokens in one batch.
@@ -192,6 +208,7 @@ pkv_status paged_attention_decode(
  *   query_start    int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
  *                  query_start[num_seqs] = num_tokens
  *   max_query_len  an upper bound of every n_s (sizes the launch)
+ *   p_format       PKV_P_HILO or PKV_P_F16 (see pkv_p_format)
  *
  * Extra shape limits: num_q_heads / num_kv_heads <= 128; block_size 8, 16 or
  * 32 (the tiles are staged in 128-byte-swizzled shared memory whose 1 KiB
@@ -210,7 +227,7 @@ pkv_status paged_attention_chunked(
     int max_blocks, const int32_t *context_lens, const int32_t *query_start,
     int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
     int num_kv_heads, int head_dim, int block_size, int num_blocks,
-    float scale, pkv_stream_t stream);
+    float scale, pkv_p_format p_format, pkv_stream_t stream);
 
 /*
  * Scratch bytes paged_attention_decode needs, with

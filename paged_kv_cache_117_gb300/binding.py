@@ -24,6 +24,7 @@ FLAG_SLOT_RANGE = 0x2
 FLAG_PAIR_RANGE = 0x4
 FLAG_LEN_RANGE = 0x8
 FLAG_TIMEOUT = 0x10
+FLAG_V_RANGE = 0x20
 
 EXPORTED_SYMBOLS = (
     "paged_kv_write",
@@ -91,7 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.paged_attention_decode_noalloc.restype = ci
     i64, i32p, i64p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
     lib.paged_attention_chunked.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, vp, ci, ci, ci,
-                                            ci, ci, ci, ci, ci, ctypes.c_float, vp]
+                                            ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
     lib.paged_attention_chunked.restype = ci
     lib.pkv_bm_create.argtypes = [ci, ci, vp]
     lib.pkv_bm_create.restype = vp
@@ -253,13 +254,18 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
     return out
 
 
+P_FORMATS = {"hilo": 0, "f16": 1}
+
+
 def paged_attention_chunked(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
-                            scale, max_query_len=None, stream=None):
+                            scale, max_query_len=None, p_format="hilo", stream=None):
     """Multi-query attention (chunked prefill and decode in one batch): out
     [T, Hq, D] from q [T, Hq, D], rows packed by sequence as query_start
     (int32 [S + 1]) says, each sequence's rows being its last positions.
     ``max_query_len`` bounds every sequence's row count; when omitted it is
-    read from query_start (a device-to-host copy)."""
+    read from query_start (a device-to-host copy).  ``p_format``: "hilo" (P as
+    hi + lo 16-bit operands, ~1e-5) or "f16" (P and V as f16, half the P.V
+    work)."""
     _need_cuda("paged_attention_chunked", out, q, k_cache, v_cache, block_tables, context_lens,
                query_start)
     N, B, Hkv, D = _cache_dims(k_cache)
@@ -276,7 +282,7 @@ def paged_attention_chunked(out, q, k_cache, v_cache, block_tables, context_lens
         _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables), int(block_tables.shape[1]),
         _ptr(context_lens), _ptr(query_start), S, T, int(max_query_len), Hq, Hkv, D, B, N,
-        float(scale), _stream(stream))
+        float(scale), P_FORMATS.get(p_format, -1), _stream(stream))
     _check("paged_attention_chunked", st)
     return out
 

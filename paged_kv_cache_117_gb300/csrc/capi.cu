@@ -310,7 +310,8 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
                                    int num_seqs, int num_tokens, int max_query_len,
                                    int num_q_heads, int num_kv_heads, int head_dim,
                                    int block_size, int num_blocks, float scale,
-                                   pkv_stream_t stream) {
+                                   pkv_p_format p_format, pkv_stream_t stream) {
+  if (p_format != PKV_P_HILO && p_format != PKV_P_F16) return PKV_ERR_DTYPE;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
     return PKV_ERR_RANGE;
@@ -382,6 +383,7 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
   p.tile_tokens = tile_tokens;
   p.num_qtiles = (int)qtiles;
   p.num_qpairs = (int)((qtiles + 1) / 2);
+  p.p_format = (int)p_format;
   p.max_query_len = max_query_len;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;

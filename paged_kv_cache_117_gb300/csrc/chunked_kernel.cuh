@@ -29,14 +29,15 @@
 // commit tracks every earlier MMA of its thread, so when S_x is seen
 // complete, the previous P_x V (and so O_x) is complete too.
 //
-// Warp roles (320 threads): warps 0-7 are two softmax warpgroups; thread t of
+// Warp roles (384 threads; 448 when V is converted): warps 0-7 are two softmax warpgroups; thread t of
 // warpgroup wg owns query row t % 128 (TMEM lane) and key columns wg*64 ..
 // wg*64+63 of every tile of both query tiles, the two threads of a row
 // agreeing on its maximum through shared memory once per tile.  Warp 8
 // issues the TMA loads (the two Q tiles once; K and V tiles through rings,
 // one box per 16 tokens of a block and 64 dims, the block-table entries
 // fetched a group of 32 ahead).  Warp 9 allocates TMEM and issues the MMAs
-// (one lane).  All hand-offs are mbarriers; every wait is bounded and a
+// (one lane).  Warps 10-13 convert V tiles to f16 when P goes in as f16 and
+// the cache is bf16 (otherwise warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is bounded and a
 // timeout sets PKV_FLAG_TIMEOUT, after which each role stops issuing and
 // drains what it has in flight before the CTA frees its TMEM and exits.
 //
@@ -56,9 +57,13 @@ namespace pkv {
 
 constexpr int CK_ROWS = 128;     // query rows per tile (MMA M)
 constexpr int CK_BN = 128;       // keys per KV tile
-constexpr int CK_THREADS = 320;
 constexpr int CK_PRODUCER = 8;   // warp ids
 constexpr int CK_MMA = 9;
+constexpr int CK_CONV = 10;      // first V-converting warp (f16 P from a bf16 cache)
+// Threads: 8 softmax warps, the TMA warp, the MMA warp and the converting
+// warps -- four (one per SM sub-partition) when a bf16 V tile is converted to
+// f16, two otherwise (then idle).
+__host__ __device__ constexpr int ck_threads(bool convert) { return convert ? 448 : 384; }
 constexpr int CK_KST = 3;        // K ring stages
 constexpr int CK_VST = 2;        // V ring stages
 constexpr float CK_SLACK = 8.0f; // lazy rescale threshold (log2 domain)
@@ -95,7 +100,8 @@ enum : int {
   CB_PF = CB_SF + 2,         // P_x written [2] (8 arrivals)
   CB_OF = CB_PF + 2,         // O_x final [2] (MMA commit)
   CB_PAIR = CB_OF + 2,       // row-statistics exchange of warps w and w + 4 [4] (64 arrivals)
-  CB_COUNT = CB_PAIR + 4,
+  CB_VC = CB_PAIR + 4,       // V stage converted to f16 [CK_VST] (one arrival per converting thread)
+  CB_COUNT = CB_VC + CK_VST,
 };
 
 // Every lane of the warp waits; the result is the same on all lanes.
@@ -128,14 +134,19 @@ __device__ __forceinline__ void store_row32(void *out, size_t base, int out_dtyp
   }
 }
 
-template <typename T, int D, int B>
-__global__ void __launch_bounds__(CK_THREADS, 1)
+template <typename T, int D, int B, bool P16>
+__global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat16>::value), 1)
     chunked_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const ChunkedParams p) {
   using C = ChunkCfg<D>;
   static_assert(CB_COUNT <= C::NBAR, "mbarrier slots");
   constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  // P16: P enters P.V as one f16 MMA operand (instead of hi + lo halves of the
+  // cache dtype); a bf16 V tile is then converted to f16 in shared memory.
+  constexpr bool CONVERT = P16 && BF16;
+  constexpr int NT = ck_threads(CONVERT);
+  constexpr int NCONV = NT - CK_CONV * 32;       // converting threads
   constexpr int BT = B < 16 ? B : 16;          // tokens per TMA box
   static_assert(BT * 128 % 1024 == 0, "boxes land on 1 KiB boundaries (128-byte swizzle atoms)");
   constexpr int BLOCKS_PER_TILE = CK_BN / B;
@@ -204,13 +215,14 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
       mbar_init(bar(CB_OF + x), 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(CB_PAIR + i), 64);
+    for (int i = 0; i < CK_VST; ++i) mbar_init(bar(CB_VC + i), NCONV);
     fence_barrier_init();
   }
   // rows of the Q tiles that no token fills (G not dividing 128) are zero
   const int q_rows = TQ * G;
   if (q_rows < CK_ROWS) {
     const int per = (CK_ROWS - q_rows) * 8;    // 16-byte chunks per half-tile
-    for (int x = tid; x < 2 * C::NH * per; x += CK_THREADS) {
+    for (int x = tid; x < 2 * C::NH * per; x += NT) {
       const int h = x / per, rem = x % per;    // h: (tile, column half)
       *reinterpret_cast<uint4 *>(sm + C::OFF_Q + h * C::HALF + (q_rows + rem / 8) * 128 +
                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
     // Order: S_A(0), S_B(0); then per KV tile j: P_A(j) V(j), S_A(j+1),
     // P_B(j) V(j), S_B(j+1).
     constexpr uint32_t ID_S = tc::idesc_f16(BF16, CK_ROWS, CK_BN, false);
-    constexpr uint32_t ID_PV = tc::idesc_f16(BF16, CK_ROWS, D, true);
+    constexpr uint32_t ID_PV = tc::idesc_f16(BF16 && !P16, CK_ROWS, D, true);
     auto issue_s = [&](int x, int j) {           // S_x(j); K(j) has landed
       if (lane == 0) {
         const uint32_t qa = sb + C::OFF_Q + x * C::Q_BYTES;
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
         for (int k = 0; k < CK_BN / 16; ++k) {
           const uint64_t bv = tc::sdesc_sw128(va + (uint32_t)k * 2048u, C::HALF, 1024);
           tc::mma_f16_ts(t0 + C::COL_O, t0 + 8u * k, bv, ID_PV, (j > 0 || k > 0) ? 1u : 0u);
-          tc::mma_f16_ts(t0 + C::COL_O, t0 + C::COL_PL + 8u * k, bv, ID_PV, 1u);
+          if (!P16) tc::mma_f16_ts(t0 + C::COL_O, t0 + C::COL_PL + 8u * k, bv, ID_PV, 1u);
         }
         if (j == nk[x] - 1) tc::commit(bar(CB_OF + x));
       }
@@ -352,12 +364,12 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
       __syncwarp();
     }
     for (int j = 0; j < nkv && ok; ++j) {
-      if (!warp_wait(bar(CB_VF + j % CK_VST), (uint32_t)(j / CK_VST) & 1u) ||
+      if (!warp_wait(bar((CONVERT ? CB_VC : CB_VF) + j % CK_VST), (uint32_t)(j / CK_VST) & 1u) ||
           !warp_wait(bar(CB_PF + 0), (uint32_t)j & 1u)) {
         ok = false;
         break;
       }
-      if (j == tail_tile) {
+      if (!CONVERT && j == tail_tile) {
         // V rows past the sequence hold whatever the pool holds there; their
         // probabilities are exactly zero, but 0 * NaN is not, so zero them
         const int z0 = L - j * CK_BN;
@@ -395,6 +407,47 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
     // waits give up in their turn)
     for (int x = 0; x < ntile; ++x) warp_wait(bar(CB_OF + x), 0);
     if (!ok && lane == 0) atomicOr(p.flags, PKV_FLAG_TIMEOUT);
+  } else if (warp >= CK_CONV) {
+    // ------------------------------------------------------------ V to f16
+    // (P16 with a bf16 cache only.)  Each V tile is converted in place, 16
+    // bytes at a time (the swizzle only moves whole 16-byte chunks, so a chunk
+    // converts where it lies); rows past the sequence become zeros.  f16 holds
+    // every bf16 value of magnitude 2^-14 .. 65504 exactly; smaller ones lose
+    // at most 2^-25 absolutely; larger ones saturate to +-65504 and are flagged
+    // (NaN stays NaN).
+    if constexpr (CONVERT) {
+      const int ct = tid - CK_CONV * 32;           // 0..NCONV-1
+      uint32_t vmax = 0;                           // largest |V| met, as bf16 bits
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int vs = j % CK_VST;
+        if (!warp_wait(bar(CB_VF + vs), (uint32_t)(j / CK_VST) & 1u)) { ok = false; break; }
+        unsigned char *vsm = sm + C::OFF_V + vs * C::KV_BYTES;
+        const int live = min(CK_BN, L - j * CK_BN);  // rows holding tokens of the sequence
+#pragma unroll 4
+        for (int c = ct; c < CK_BN * 8 * C::NH; c += NCONV) {
+          const int h = c / (CK_BN * 8), rem = c % (CK_BN * 8), r = rem / 8;
+          uint4 *ptr = reinterpret_cast<uint4 *>(vsm + h * C::HALF + r * 128 + (rem % 8) * 16);
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (r < live) {
+            w = *ptr;
+            uint32_t *ww = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // largest magnitude seen (bf16 bits without the sign, both halves)
+              vmax = max(vmax, max(ww[e] & 0x7fffu, (ww[e] >> 16) & 0x7fffu));
+              const float2 f = Widen<__nv_bfloat16>::pair(ww[e]);
+              asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(ww[e]) : "f"(f.y), "f"(f.x));
+            }
+          }
+          *ptr = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(CB_VC + vs));
+      }
+      // bf16 magnitudes above 65504 (0x477f) became +-65504
+      if (vmax > 0x477fu) atomicOr(p.flags, PKV_FLAG_V_RANGE);
+      if (!ok && lane == 0) atomicOr(p.flags, PKV_FLAG_TIMEOUT);
+    }
   } else {
     // ------------------------------------------------------------ softmax
     // Per KV tile j: tile A, then tile B (when it needs tile j).
@@ -457,7 +510,9 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
           alpha = fast_exp2(m[x] - mnew);
           m[x] = mnew;
         }
-        // P = exp2(s * scale * log2 e - m) as hi + lo 16-bit pairs
+        // P = exp2(s * scale * log2 e - m): as hi + lo pairs of the cache
+        // dtype, or (P16) as f16 pairs with the row sum taken over the
+        // rounded values (each output row is then an exact convex combination)
         const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m[x], -m[x]);
         float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t hiw[HC / 2], low[HC / 2];
@@ -466,10 +521,16 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
           const float2 v = fma2(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                                 sl2x2, negm);
           const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
-          lsum[e & 1] = make_float2(lsum[e & 1].x + pe.x, lsum[e & 1].y + pe.y);
-          hiw[e] = Mma<T>::pack(pe.x, pe.y);
-          const float2 hf = Widen<T>::pair(hiw[e]);
-          low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
+          if constexpr (P16) {
+            hiw[e] = Mma<__half>::pack(pe.x, pe.y);
+            const float2 hf = Widen<__half>::pair(hiw[e]);
+            lsum[e & 1] = make_float2(lsum[e & 1].x + hf.x, lsum[e & 1].y + hf.y);
+          } else {
+            lsum[e & 1] = make_float2(lsum[e & 1].x + pe.x, lsum[e & 1].y + pe.y);
+            hiw[e] = Mma<T>::pack(pe.x, pe.y);
+            const float2 hf = Widen<T>::pair(hiw[e]);
+            low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
+          }
         }
         l[x] = l[x] * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
         // O_x is quiet: the P_x V before this S_x has completed
@@ -486,7 +547,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
           }
         }
         tc::st_32x32b_x32(tt + (uint32_t)(wg * (HC / 2)), hiw);
-        tc::st_32x32b_x32(tt + C::COL_PL + (uint32_t)(wg * (HC / 2)), low);
+        if (!P16) tc::st_32x32b_x32(tt + C::COL_PL + (uint32_t)(wg * (HC / 2)), low);
         tc::wait_st();
         tc::fence_before_sync();
         __syncwarp();
@@ -524,19 +585,28 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
 
 // ---- host side ---------------------------------------------------------------
 
-template <typename T, int D, int B>
-cudaError_t launch_chunked_cfg(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                               const CUtensorMap &vmap, const ChunkedParams &p,
-                               cudaStream_t stream) {
+template <typename T, int D, int B, bool P16>
+cudaError_t launch_chunked_p(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, const ChunkedParams &p,
+                             cudaStream_t stream) {
   using C = ChunkCfg<D>;
-  auto kern = chunked_kernel<T, D, B>;
+  auto kern = chunked_kernel<T, D, B, P16>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_qpairs * p.num_seqs * p.num_kv_heads;
   if (units <= 0) return cudaSuccess;
-  return launch_pdl(kern, dim3((unsigned)units), dim3(CK_THREADS), (size_t)C::SMEM, stream, qmap,
+  constexpr int NT = ck_threads(P16 && std::is_same<T, __nv_bfloat16>::value);
+  return launch_pdl(kern, dim3((unsigned)units), dim3(NT), (size_t)C::SMEM, stream, qmap,
                     kmap, vmap, p);
+}
+
+template <typename T, int D, int B>
+cudaError_t launch_chunked_cfg(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, const ChunkedParams &p,
+                               cudaStream_t stream) {
+  return p.p_format == PKV_P_F16 ? launch_chunked_p<T, D, B, true>(qmap, kmap, vmap, p, stream)
+                                 : launch_chunked_p<T, D, B, false>(qmap, kmap, vmap, p, stream);
 }
 
 template <typename T, int D>

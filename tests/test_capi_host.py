@@ -103,12 +103,12 @@ def test_decode_validation(lib):
 def chunked(lib, **kw):
     a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
              max_blocks=4, lens=fake(5), qs=fake(6), S=2, T=64, maxq=32, Hq=8, Hkv=2, D=128,
-             B=16, N=8, scale=0.1)
+             B=16, N=8, scale=0.1, pf=0)
     a.update(kw)
     return lib.paged_attention_chunked(a["out"], a["out_dt"], a["q"], a["k"], a["v"], a["dt"],
                                        a["tab"], a["max_blocks"], a["lens"], a["qs"], a["S"],
                                        a["T"], a["maxq"], a["Hq"], a["Hkv"], a["D"], a["B"],
-                                       a["N"], a["scale"], None)
+                                       a["N"], a["scale"], a["pf"], None)
 
 
 def test_chunked_validation(lib):
@@ -116,6 +116,7 @@ def test_chunked_validation(lib):
     assert chunked(lib, qs=None) == NULL
     assert chunked(lib, dt=F32) == DTYPE
     assert chunked(lib, out_dt=7) == DTYPE
+    assert chunked(lib, pf=2) == DTYPE
     assert chunked(lib, D=96) == SHAPE
     assert chunked(lib, B=12) == SHAPE
     assert chunked(lib, B=4) == SHAPE

@@ -20,7 +20,8 @@ def _w(Hq, Hkv, D, B, dtype=torch.bfloat16, N=400, seed=500):
     return wl.Workload("chunk_case", 0, Hq, Hkv, D, B, N, dtype, 0, seed, "fixed", ())
 
 
-def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None):
+def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None, p_format="hilo",
+         v_spike=None):
     import paged_kv_cache_117_gb300 as pkv
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
@@ -34,6 +35,8 @@ def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None):
     g = torch.Generator().manual_seed(w.seed + 77)
     q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g).to(w.dtype)
     key, val = wl.make_rows(w, 0, T)
+    if v_spike is not None:   # one new V value far outside the f16 range
+        val[0, 0, 0] = v_spike
     kd, vd = k.cuda(), v.cuda()
     ops.write_kv(k, v, key, val, step.slots)
     ref = ops.attend_chunked(q, k, v, step.tables, step.lens, step.query_start, w.scale)
@@ -43,9 +46,13 @@ def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None):
     pkv.paged_attention_chunked(out, q.cuda(), kd, vd, wl.pad_tables(step.tables, step.width).cuda(),
                                 torch.tensor(step.lens, dtype=torch.int32, device="cuda"),
                                 torch.tensor(step.query_start, dtype=torch.int32, device="cuda"),
-                                w.scale, max_query_len=max(counts))
+                                w.scale, max_query_len=max(counts), p_format=p_format)
     torch.cuda.synchronize()
-    assert pkv.read_device_flags(clear=True) == 0
+    flags = pkv.read_device_flags(clear=True)
+    if v_spike is not None:
+        assert flags == pkv.FLAG_V_RANGE and torch.isfinite(out).all()
+        return None, step
+    assert flags == 0
     assert torch.equal(kd.cpu().view(torch.int16), k.view(torch.int16))
     assert torch.equal(vd.cpu().view(torch.int16), v.view(torch.int16))
     return gh.assert_close_to_oracle(out, ref, ATOL), step
@@ -146,3 +153,30 @@ def test_prefill_full_size_sampled():
             ref = ops.attend(qc[r0 + i:r0 + i + 1], kb, vb, [[remap[b] for b in step.tables[s]]],
                              [p + 1], w.scale)
             gh.assert_close_to_oracle(out[r0 + i:r0 + i + 1], ref, ATOL)
+
+
+# ---- P as one f16 operand (V converted to f16 for a bf16 cache) -------------
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 1), (10, 2), (64, 1)])
+def test_f16_p_group_sizes(hq, hkv):
+    _run(_w(hq, hkv, 64, 16, N=300), [0, 150, 9], [97, 40, 2], p_format="f16")
+
+
+@pytest.mark.parametrize("b", [8, 16, 32])
+@pytest.mark.parametrize("d", [64, 128])
+def test_f16_p_block_and_head_dim(b, d):
+    _run(_w(8, 2, d, b, N=600), [0, 129, 300], [200, 127, 33], p_format="f16")
+
+
+def test_f16_p_f16_cache_mixed_batch_and_poison():
+    _run(_w(8, 2, 128, 16, dtype=torch.float16), [0, 200, 511, 37], [130, 129, 1, 3],
+         p_format="f16")
+    _run(_w(8, 2, 128, 16), [0, 45, 300], [77, 130, 12], poison=True, p_format="f16")
+    _run(_w(8, 2, 128, 16), [0, 0, 128, 127, 255], [128, 256, 128, 1, 129], p_format="f16",
+         out_dtype=torch.bfloat16)
+
+
+def test_f16_p_v_out_of_range_is_flagged():
+    # a V value beyond +-65504 cannot be an f16 operand: it is clamped, the
+    # output stays finite and the device flag word reports it
+    _run(_w(8, 2, 128, 16), [0, 40], [30, 20], p_format="f16", v_spike=1.0e5)
