@@ -180,3 +180,79 @@ def test_f16_p_v_out_of_range_is_flagged():
     # a V value beyond +-65504 cannot be an f16 operand: it is clamped, the
     # output stays finite and the device flag word reports it
     _run(_w(8, 2, 128, 16), [0, 40], [30, 20], p_format="f16", v_spike=1.0e5)
+
+
+def test_bad_metadata_is_flagged_not_faulted():
+    """Device-side values the kernel cannot trust: a block id outside the
+    pool is read as zeros and flagged; a length past the table is clamped and
+    flagged; a sequence with more queries than tokens, or query_start out of
+    order, is skipped (rows untouched) and flagged.  Nothing faults."""
+    import paged_kv_cache_117_gb300 as pkv
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    B, H, D, N = 16, 2, 64, 32
+    k = torch.randn((N, B, H, D), device="cuda").to(torch.bfloat16)
+    v = torch.randn((N, B, H, D), device="cuda").to(torch.bfloat16)
+    q = torch.randn((40, 8, D), device="cuda").to(torch.bfloat16)
+    tables = torch.tensor([[1, N + 5, 2], [3, 4, 5], [6, 7, 8], [9, 10, 11]],
+                          dtype=torch.int32, device="cuda")
+    # seq 0: bad block id; seq 1: length past the table (clamped to 48);
+    # seq 2: 10 queries but 5 tokens (skipped); seq 3: fine
+    lens = torch.tensor([40, 10_000, 5, 30], dtype=torch.int32, device="cuda")
+    qs = torch.tensor([0, 10, 20, 30, 40], dtype=torch.int32, device="cuda")
+    out = torch.full((40, 8, D), 7.0, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_chunked(out, q, k, v, tables, lens, qs, 0.125, max_query_len=10)
+    torch.cuda.synchronize()
+    f = pkv.read_device_flags(clear=True)
+    assert f & pkv.FLAG_BLOCK_RANGE and f & pkv.FLAG_LEN_RANGE
+    assert not f & pkv.FLAG_TIMEOUT
+    assert torch.isfinite(out).all()
+    assert (out[20:30] == 7.0).all()                # skipped rows untouched
+    # query_start running backwards: the sequence is skipped and flagged
+    qs_bad = torch.tensor([0, 10, 5, 30, 40], dtype=torch.int32, device="cuda")
+    out.fill_(7.0)
+    pkv.paged_attention_chunked(out, q, k, v, tables, torch.tensor([10, 10, 10, 30], dtype=torch.int32,
+                                device="cuda"), qs_bad, 0.125, max_query_len=25)
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) & pkv.FLAG_LEN_RANGE
+    assert torch.isfinite(out).all()
+
+
+def test_chunked_step_in_a_cuda_graph():
+    """A chunked-prefill step (write + attention) captured in one CUDA graph
+    and replayed: the call path does no host synchronisation when
+    max_query_len is given, and replays match the oracle."""
+    import paged_kv_cache_117_gb300 as pkv
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = _w(8, 2, 128, 16)
+    step = gh.plan_chunked(w, [0, 100, 37], [90, 40, 1])
+    T = step.query_start[-1]
+    k, v = wl.make_pool(w, "cpu")
+    kd, vd = k.cuda(), v.cuda()
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((T, 8, 128), generator=g).to(w.dtype)
+    key, val = wl.make_rows(w, 0, T)
+    ops.write_kv(k, v, key, val, step.slots)
+    ref = ops.attend_chunked(q, k, v, step.tables, step.lens, step.query_start, w.scale)
+    qd, keyd, vald = q.cuda(), key.cuda(), val.cuda()
+    slots = torch.tensor(step.slots, dtype=torch.int64, device="cuda")
+    tab = wl.pad_tables(step.tables).cuda()
+    lens = torch.tensor(step.lens, dtype=torch.int32, device="cuda")
+    qs = torch.tensor(step.query_start, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, 8, 128), dtype=torch.float32, device="cuda")
+    pkv.load()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            pkv.paged_kv_write(keyd, vald, kd, vd, slots)
+            pkv.paged_attention_chunked(out, qd, kd, vd, tab, lens, qs, w.scale, max_query_len=90)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkv.read_device_flags(clear=True) == 0
+        gh.assert_close_to_oracle(out, ref, ATOL)
