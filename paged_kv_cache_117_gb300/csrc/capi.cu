@@ -54,13 +54,17 @@ unsigned *device_flags() {
 // descriptors are cached per thread.
 struct MapKey {
   const void *base;
-  int dt, n, b, h, d;
+  int dt, n, b, h, d, rows;
   bool operator==(const MapKey &o) const {
-    return base == o.base && dt == o.dt && n == o.n && b == o.b && h == o.h && d == o.d;
+    return base == o.base && dt == o.dt && n == o.n && b == o.b && h == o.h && d == o.d &&
+           rows == o.rows;
   }
 };
 
-bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, int Hkv, int D) {
+// Tensor map of a K or V pool: one box = 64 dims (128 bytes, 128B-swizzled) x
+// box_rows tokens of one KV head of one block.
+bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, int Hkv, int D,
+              int box_rows) {
   struct Entry {
     MapKey key;
     CUtensorMap map;
@@ -68,7 +72,7 @@ bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, in
   };
   thread_local Entry cache[4] = {};
   thread_local int next = 0;
-  const MapKey key{base, (int)dt, N, B, Hkv, D};
+  const MapKey key{base, (int)dt, N, B, Hkv, D, box_rows};
   for (auto &e : cache)
     if (e.used && e.key == key) {
       *out = e.map;
@@ -79,8 +83,7 @@ bool pool_map(CUtensorMap *out, const void *base, pkv_dtype dt, int N, int B, in
   const cuuint64_t es = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)B, (cuuint64_t)N};
   cuuint64_t strides[3] = {D * es, (cuuint64_t)Hkv * D * es, (cuuint64_t)B * Hkv * D * es};
-  // one box = 64 dims (128 bytes, 128B-swizzled) x up to 16 tokens of one KV head
-  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)(B < 16 ? B : 16), 1u};
+  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
@@ -261,8 +264,9 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
     return PKV_ERR_ALIAS;
 
   CUtensorMap kmap, vmap;
-  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+  const int rows16 = block_size < 16 ? block_size : 16;   // decode: up to 16 tokens a box
+  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, rows16) ||
+      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, rows16))
     return cuda_fail_msg("cuTensorMapEncodeTiled failed for the KV pool");
   unsigned *flags = device_flags();
   if (!flags) return cuda_fail_msg("device flag word unavailable");
@@ -345,8 +349,11 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
     return PKV_ERR_ALIAS;
 
   CUtensorMap kmap, vmap, qmap;
-  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+  // chunked: a whole block (up to 32 tokens) a box -- fewer, larger TMA boxes
+  if (!pool_map(&kmap, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                block_size) ||
+      !pool_map(&vmap, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                block_size))
     return cuda_fail_msg("cuTensorMapEncodeTiled failed for the KV pool");
   {
     EncodeTiledFn fn = encode_fn();

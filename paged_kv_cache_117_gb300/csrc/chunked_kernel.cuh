@@ -34,7 +34,7 @@
 // wg*64+63 of every tile of both query tiles, the two threads of a row
 // agreeing on its maximum through shared memory once per tile.  Warp 8
 // issues the TMA loads (the two Q tiles once; K and V tiles through rings,
-// one box per 16 tokens of a block and 64 dims, the block-table entries
+// one box per block (all its tokens) and 64 dims, the block-table entries
 // fetched a group of 32 ahead).  Warp 9 allocates TMEM and issues the MMAs
 // (one lane).  Warps 10-13 convert V tiles to f16 when P goes in as f16 and
 // the cache is bf16 (otherwise warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is bounded and a
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   constexpr bool CONVERT = P16 && BF16;
   constexpr int NT = ck_threads(CONVERT);
   constexpr int NCONV = NT - CK_CONV * 32;       // converting threads
-  constexpr int BT = B < 16 ? B : 16;          // tokens per TMA box
+  constexpr int BT = B;                        // tokens per TMA box: a whole block
   static_assert(BT * 128 % 1024 == 0, "boxes land on 1 KiB boundaries (128-byte swizzle atoms)");
   constexpr int BLOCKS_PER_TILE = CK_BN / B;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
