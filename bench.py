@@ -5,7 +5,11 @@ One step = one pass of the whole path over one batch: the batched
 copy-on-write block copy (when the workload has copies), the KV write of every
 sequence's new token, and decode attention (partitioned pass + merge) -- all
 through the library's C ABI.  Inputs are resident in HBM when timing starts;
-L2 is flushed (256 MiB write) before every timed step, outside the timed span.
+L2 is flushed before every timed step, outside the timed span: a 256 MiB
+buffer is written (evicting what the last step left in L2), then another
+256 MiB buffer is read, so that the flush's own dirty lines are written back
+before the timed span starts rather than inside it (a write-only flush adds
+~15 us of write-back to a ~230 us decode call).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
@@ -37,6 +41,25 @@ FLUSH_BYTES = 256 << 20
 TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
                       "shared": 2048, "beam": 2048, "prefill": 8192, "prefix": 4096}
 SHARING = ("shared", "beam")   # workloads whose sequences share blocks
+
+
+L2_NOTE = ("flushed before every step, outside the timed span: 256 MiB written, then another "
+           "256 MiB read so the flush's dirty lines are written back before the span")
+
+
+class L2Flush:
+    """Evicts L2 between timed iterations: writes one buffer larger than L2,
+    then reads a second one, leaving L2 full of clean lines that no kernel of
+    the step reads."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink.add_(self.r.sum())
 
 
 def parse_args():
@@ -480,7 +503,7 @@ def run_native(a, world, rank, local):
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
     wss = [ws] + [torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
                   for _ in range(1, a.layers)]
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0],
                                tables if w.lens_kind in SHARING else None)
     # block copy (when there are pairs) + KV write + work list + attention, per layer
@@ -515,7 +538,7 @@ def run_native(a, world, rank, local):
                 d1.record(stream)
 
     for _ in range(max(3, a.warmup)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert pkv.read_device_flags(clear=True) == 0
@@ -535,7 +558,7 @@ def run_native(a, world, rank, local):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s0, s1, d0, d1 in evs:
-        flush.zero_()
+        flush()
         s0.record(stream)
         if graph is not None:
             graph.replay()
@@ -549,7 +572,7 @@ def run_native(a, world, rank, local):
     step_ms = sum(s0.elapsed_time(s1) for s0, s1, _, _ in evs) / K
     if graph is not None:   # layer 0's attention call, timed eagerly for the roofline
         for _, _, d0, d1 in evs:
-            flush.zero_()
+            flush()
             d0.record(stream)
             pkv.paged_attention_decode(out, q, k, v, tab, lens_t, w.scale, partition_tokens=pt,
                                        workspace=ws)
@@ -595,7 +618,7 @@ def run_native(a, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     for e0, e1 in e2e_evs:
-        flush.zero_()
+        flush()
         e0.record(stream)
         e2e_step()
         e1.record(stream)
@@ -615,7 +638,7 @@ def run_native(a, world, rank, local):
         "data": "synthetic",
         "config": {"workload": workload_desc(w, width), "partition_tokens": pt,
                    "out_dtype": str(out.dtype).replace("torch.", ""),
-                   "l2": "flushed before every step (256 MiB write, outside the timed span)",
+                   "l2": L2_NOTE,
                    "layers": a.layers, "cuda_graph": bool(a.graph),
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "pct_of_peak": round(100 * value_gbs / world / peak, 1),
@@ -702,7 +725,7 @@ def run_native_chunked(a, world, rank, local):
     tab, lens_t, qs_t, slots = (x.to(dev) for x in (tab_cpu, lens_cpu, qs_cpu, slots_cpu))
     maxq = max(counts)
     out = torch.empty((T, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     flops = chunked_flops(w, lens, counts)
 
     cpu = None
@@ -730,7 +753,7 @@ def run_native_chunked(a, world, rank, local):
             d1.record(stream)
 
     for _ in range(max(3, a.warmup)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert pkv.read_device_flags(clear=True) == 0
@@ -743,7 +766,7 @@ def run_native_chunked(a, world, rank, local):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s0, s1, d0, d1 in evs:
-        flush.zero_()
+        flush()
         s0.record(stream)
         step(d0, d1)
         s1.record(stream)
@@ -782,7 +805,7 @@ def run_native_chunked(a, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     for e0, e1 in e2e_evs:
-        flush.zero_()
+        flush()
         e0.record(stream)
         e2e_step()
         e1.record(stream)
@@ -799,7 +822,7 @@ def run_native_chunked(a, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": desc, "out_dtype": "bfloat16", "p_format": a.p_format,
-                   "l2": "flushed before every step (256 MiB write, outside the timed span)",
+                   "l2": L2_NOTE,
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "tokens_per_s": round(world * T / (step_ms * 1e-3), 1),
         "attention_ms": round(dec_ms, 4),

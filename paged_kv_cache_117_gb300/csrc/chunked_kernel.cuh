@@ -147,8 +147,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   constexpr bool CONVERT = P16 && BF16;
   constexpr int NT = ck_threads(CONVERT);
   constexpr int NCONV = NT - CK_CONV * 32;       // converting threads
-  constexpr int BT = B;                        // tokens per TMA box: a whole block
-  static_assert(BT * 128 % 1024 == 0, "boxes land on 1 KiB boundaries (128-byte swizzle atoms)");
+  static_assert(B * 128 % 1024 == 0, "boxes land on 1 KiB boundaries (128-byte swizzle atoms)");
   constexpr int BLOCKS_PER_TILE = CK_BN / B;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *sm = smem_raw;
@@ -243,7 +242,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop: lane i holds block-table entry i of the
     // current group of 32 (TPG tiles), the next group's entries are already
-    // in flight, and lane 0 issues the TMA loads.
+    // in flight, and the lanes issue the TMA loads.
     constexpr int TPG = 32 / BLOCKS_PER_TILE;    // tiles per group of 32 entries
     const int32_t *tbl = p.block_tables + (size_t)s * p.max_blocks;
     const int nb_used = min(nb_valid, nkv * BLOCKS_PER_TILE);
@@ -267,16 +266,19 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
           tma_load_3d(sb + C::OFF_Q + x * C::Q_BYTES + h * C::HALF, &qmap, h * 64, kvh * G,
                       q0 + tb[x], bar(CB_Q));
     }
+    // one TMA box per (block, 64-dim half) of the tile, lane i issuing box i
+    // (issuing them from one lane in turn is a little slower)
+    static_assert(BLOCKS_PER_TILE * C::NH <= 32, "one box per lane");
     auto load_tile = [&](const CUtensorMap *map, uint32_t dst, const int (&blk)[BLOCKS_PER_TILE],
                          uint32_t full) {
+      if (lane < BLOCKS_PER_TILE * C::NH) {
+        const int b = lane / C::NH, h = lane % C::NH;
+        int bb = blk[0];
 #pragma unroll
-      for (int b = 0; b < BLOCKS_PER_TILE; ++b)
-#pragma unroll
-        for (int sub = 0; sub < B / BT; ++sub)
-#pragma unroll
-          for (int h = 0; h < C::NH; ++h)
-            tma_load_4d_keep(dst + h * C::HALF + (b * B + sub * BT) * 128, map, h * 64, kvh,
-                             sub * BT, blk[b], full);
+        for (int i = 1; i < BLOCKS_PER_TILE; ++i)
+          if (b == i) bb = blk[i];
+        tma_load_4d_keep(dst + h * C::HALF + b * B * 128, map, h * 64, kvh, 0, bb, full);
+      }
     };
     int cur = fetch(0), nxt = fetch(1);
     int nk_issued = 0, nv_issued = 0;
@@ -294,19 +296,17 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
         ok = false;
         break;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(CB_KF + ks), (uint32_t)C::KV_BYTES);
-        load_tile(&kmap, sb + C::OFF_K + ks * C::KV_BYTES, blk, bar(CB_KF + ks));
-      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(CB_KF + ks), (uint32_t)C::KV_BYTES);
+      __syncwarp();
+      load_tile(&kmap, sb + C::OFF_K + ks * C::KV_BYTES, blk, bar(CB_KF + ks));
       nk_issued = j + 1;
       if (j >= CK_VST && !warp_wait(bar(CB_VE + vs), ((uint32_t)(j / CK_VST) & 1u) ^ 1u)) {
         ok = false;
         break;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(CB_VF + vs), (uint32_t)C::KV_BYTES);
-        load_tile(&vmap, sb + C::OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
-      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(CB_VF + vs), (uint32_t)C::KV_BYTES);
+      __syncwarp();
+      load_tile(&vmap, sb + C::OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
       nv_issued = j + 1;
     }
     // drain: every load issued has landed before the CTA may exit (loads
