@@ -76,6 +76,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step: one K/V pool per layer, shared block tables")
+    ap.add_argument("--kv-write", choices=["append", "separate"], default="append",
+                    help="decode workloads: the step's KV write inside the attention call "
+                         "(paged_attention_decode_append) or as its own kernel (paged_kv_write "
+                         "then paged_attention_decode)")
     ap.add_argument("--p-format", choices=["hilo", "f16"], default="hilo",
                     help="chunked workloads: P as hi + lo 16-bit operands, or as one f16 operand")
     ap.add_argument("--graph", action="store_true",
@@ -292,7 +296,7 @@ def sources_sha256(sources):
 
 
 def measured_traffic(workload, partition_tokens, profile="decode_kernel_llama8b.md",
-                     sources=DECODE_SOURCES):
+                     sources=DECODE_SOURCES, kv_write=None):
     """DRAM bytes per launch from a committed ncu summary, or None when it was
     taken on another workload or the kernel's sources changed since."""
     try:
@@ -300,6 +304,7 @@ def measured_traffic(workload, partition_tokens, profile="decode_kernel_llama8b.
         kv = dict(line.split(": ", 1) for line in text.splitlines()
                   if line.startswith(("traffic_", "source_sha256")))
         if (kv.get("source_sha256") == sources_sha256(sources)
+                and kv.get("traffic_kv_write", "separate") == (kv_write or "separate")
                 and kv.get("traffic_workload") == workload
                 and int(kv.get("traffic_partition_tokens", -1)) == partition_tokens):
             return int(kv["traffic_bytes_per_launch"])
@@ -506,8 +511,10 @@ def run_native(a, world, rank, local):
     flush = L2Flush(dev)
     nbytes = algorithmic_bytes(w, lens, width, pt, out.element_size(), pairs.shape[0],
                                tables if w.lens_kind in SHARING else None)
-    # block copy (when there are pairs) + KV write + work list + attention, per layer
-    launches_per_step = a.layers * ((1 if pairs.shape[0] else 0) + 1 + 2)
+    # block copy (when there are pairs) + KV write (its own kernel unless
+    # appended by the attention call) + work list + attention, per layer
+    fused = a.kv_write == "append"
+    launches_per_step = a.layers * ((1 if pairs.shape[0] else 0) + (0 if fused else 1) + 2)
 
     # CPU-oracle sample: inputs snapshot before any library kernel runs
     cpu = None
@@ -525,15 +532,28 @@ def run_native(a, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
+    if fused:   # the call derives each new token's slot from the tables
+        B = w.block_size
+        for s_, (t_, L_) in enumerate(zip(tables, lens)):
+            assert int(slots_cpu[s_]) == (t_[(L_ - 1) // B] * B + (L_ - 1) % B if L_ else -1)
+
+    def attend(o, ql, keyl, vall, kl, vl, tb, ln, wsl):
+        if fused:
+            pkv.paged_attention_decode_append(o, ql, keyl, vall, kl, vl, tb, ln, w.scale,
+                                              partition_tokens=pt, workspace=wsl)
+        else:
+            pkv.paged_attention_decode(o, ql, kl, vl, tb, ln, w.scale, partition_tokens=pt,
+                                       workspace=wsl)
+
     def step(d0=None, d1=None):
         for li, (kl, vl, ql, keyl, vall) in enumerate(layers):
             if pairs.shape[0]:
                 pkv.paged_block_copy(kl, vl, pairs)
-            pkv.paged_kv_write(keyl, vall, kl, vl, slots)
+            if not fused:
+                pkv.paged_kv_write(keyl, vall, kl, vl, slots)
             if li == 0 and d0 is not None:
                 d0.record(stream)
-            pkv.paged_attention_decode(outs[li] if li else out, ql, kl, vl, tab, lens_t,
-                                       w.scale, partition_tokens=pt, workspace=wss[li])
+            attend(outs[li] if li else out, ql, keyl, vall, kl, vl, tab, lens_t, wss[li])
             if li == 0 and d1 is not None:
                 d1.record(stream)
 
@@ -574,8 +594,7 @@ def run_native(a, world, rank, local):
         for _, _, d0, d1 in evs:
             flush()
             d0.record(stream)
-            pkv.paged_attention_decode(out, q, k, v, tab, lens_t, w.scale, partition_tokens=pt,
-                                       workspace=ws)
+            attend(out, q, key, value, k, v, tab, lens_t, ws)
             d1.record(stream)
         torch.cuda.synchronize()
     dec_ms = sum(d0.elapsed_time(d1) for _, _, d0, d1 in evs) / K
@@ -583,16 +602,18 @@ def run_native(a, world, rank, local):
     dec_ms = max_over_ranks(world, dec_ms, dev)
 
     # end to end: each step's inputs (q, new K/V rows, block tables, lengths,
-    # slot mapping) arrive in one pinned host staging buffer and go to the
-    # device in one copy; the result comes back in one copy
-    parts = [q, key, value, tab, lens_t, slots, pairs]
+    # slot mapping -- not needed when the attention call appends -- and copy
+    # pairs) arrive in one pinned host staging buffer and go to the device in
+    # one copy; the result comes back in one copy
+    slots_e, slots_cpu_e = (slots[:0], slots_cpu[:0]) if fused else (slots, slots_cpu)
+    parts = [q, key, value, tab, lens_t, slots_e, pairs]
     sizes = [t.numel() * t.element_size() for t in parts]
     offs = [0]
     for n in sizes:
         offs.append(offs[-1] + (n + 255) // 256 * 256)
     h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
     d_in = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
-    for t, o, n in zip((q, key, value, tab_cpu, lens_cpu, slots_cpu, pairs_cpu), offs, sizes):
+    for t, o, n in zip((q, key, value, tab_cpu, lens_cpu, slots_cpu_e, pairs_cpu), offs, sizes):
         if n:
             h_in[o:o + n].copy_(t.cpu().contiguous().view(torch.uint8).view(-1))
     views = [d_in[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
@@ -605,9 +626,9 @@ def run_native(a, world, rank, local):
         d_in.copy_(h_in, non_blocking=True)
         if pairs.shape[0]:
             pkv.paged_block_copy(k, v, e_pairs)
-        pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
-        pkv.paged_attention_decode(out, e_q, k, v, e_tab, e_lens, w.scale, partition_tokens=pt,
-                                   workspace=ws)
+        if not fused:
+            pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
+        attend(out, e_q, e_key, e_val, k, v, e_tab, e_lens, ws)
         h_out.copy_(out, non_blocking=True)
 
     if a.layers != 1:   # the end-to-end leg times the single-layer step only
@@ -628,7 +649,10 @@ def run_native(a, world, rank, local):
     assert pkv.read_device_flags(clear=True) == 0
 
     peak, peak_kind = peak_hbm()
-    achieved = nbytes["attention"] / (dec_ms * 1e-3) / 1e9
+    # the timed call's algorithmic bytes: the attention's, plus the new rows
+    # read and stored when it appends them
+    call_bytes = nbytes["attention"] + (nbytes["write"] if fused else 0)
+    achieved = call_bytes / (dec_ms * 1e-3) / 1e9
     value_gbs = world * a.layers * nbytes["step"] / (step_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": UNIT, "n_gpus": world,
@@ -638,7 +662,7 @@ def run_native(a, world, rank, local):
         "data": "synthetic",
         "config": {"workload": workload_desc(w, width), "partition_tokens": pt,
                    "out_dtype": str(out.dtype).replace("torch.", ""),
-                   "l2": L2_NOTE,
+                   "l2": L2_NOTE, "kv_write": a.kv_write,
                    "layers": a.layers, "cuda_graph": bool(a.graph),
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "pct_of_peak": round(100 * value_gbs / world / peak, 1),
@@ -647,11 +671,13 @@ def run_native(a, world, rank, local):
         "bytes_per_step": nbytes,
         **({"unique_kv_gbs": round(world * a.layers * (nbytes["step"] - nbytes["kv"] + nbytes["kv_unique"])
                                    / (step_ms * 1e-3) / 1e9, 1)} if "kv_unique" in nbytes else {}),
-        "roofline": {"kernel": "paged_attention_decode (work list + attention with fused merge)",
+        "roofline": {"kernel": ("paged_attention_decode_append (work list + KV write, attention "
+                                "and merge in one pass)" if fused else
+                                "paged_attention_decode (work list + attention with fused merge)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": measured_traffic(w.name, pt)},
+                     "traffic": measured_traffic(w.name, pt, kv_write=a.kv_write)},
         "e2e": ({"value": round(world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                  "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h} if e2e_ms else None),

@@ -10,6 +10,9 @@
  *                           the block manager assigned ("reshape and cache")
  *   paged_block_copy        the batched copy-on-write block copy
  *   paged_attention_decode  single-query attention over the paged context
+ *   paged_attention_decode_append
+ *                           the step's KV write and decode attention in one
+ *                           call
  *   paged_attention_chunked multi-query attention over the paged context:
  *                           chunked prefill and decode in one batch
  *
@@ -168,6 +171,38 @@ pkv_status paged_attention_decode(
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     int num_blocks, float scale, int partition_tokens, void *workspace,
     size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * paged_attention_decode_append -- the decode step's KV write and decode
+ * attention in one call.
+ *
+ * Computes what paged_kv_write followed by paged_attention_decode computes
+ * when this step's token of sequence s (L_s = context_lens[s] >= 1 counting
+ * it) goes to position L_s - 1, i.e. to slot block_tables[s, (L_s - 1) /
+ * block_size] * block_size + (L_s - 1) % block_size ("PagedAttention",
+ * section 5: the new key and value are written first, then the query attends
+ * over every valid position including its own).  key and value hold the
+ * step's rows, [num_seqs, num_kv_heads, head_dim] of the cache dtype,
+ * 16-byte aligned, overlapping neither pool, out nor the workspace.  The
+ * attention takes position L_s - 1 from these rows directly and the call
+ * stores them into both pools, so the pools afterwards hold exactly what
+ * paged_kv_write would have left.  Sequences with L_s == 0 append nothing
+ * (zeros out); a length past the table is clamped and flagged
+ * (PKV_FLAG_LEN_RANGE) and appends nothing; a bad block id for the slot is
+ * flagged (PKV_FLAG_BLOCK_RANGE) and nothing is stored.  The slot's block
+ * must belong to sequence s alone during the call (copy-on-write done
+ * before, as the block manager guarantees): another sequence reading it in
+ * the same call would see either the old or the new row.  Every other
+ * argument, the workspace and the launches are those of
+ * paged_attention_decode.
+ */
+pkv_status paged_attention_decode_append(
+    void *out, pkv_dtype out_dtype, const void *q, const void *key,
+    const void *value, void *k_cache, void *v_cache, pkv_dtype dtype,
+    const int32_t *block_tables, int max_blocks, const int32_t *context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, int partition_tokens,
+    void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* How P (the softmax weights) enters the P.V product of
  * paged_attention_chunked; scores, the softmax and accumulation are fp32

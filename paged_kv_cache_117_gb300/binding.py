@@ -35,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "pkv_read_device_flags",
     "pkv_last_error_string",
     "paged_attention_decode_noalloc",
+    "paged_attention_decode_append",
     "paged_attention_chunked",
     "pkv_pc_create",
     "pkv_pc_add_sequence",
@@ -79,6 +80,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.paged_attention_decode.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, ci, ci, ci,
                                            ci, ci, ci, cf, ci, vp, cs, vp]
     lib.paged_attention_decode.restype = ci
+    lib.paged_attention_decode_append.argtypes = [vp, ci, vp, vp, vp, vp, vp, ci, vp, ci, vp,
+                                                  ci, ci, ci, ci, ci, ci, cf, ci, vp, cs, vp]
+    lib.paged_attention_decode_append.restype = ci
     lib.paged_attention_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
     lib.paged_attention_workspace_bytes.restype = cs
     lib.pkv_status_string.argtypes = [ci]
@@ -230,6 +234,37 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         S, Hq, Hkv, D, B, N, float(scale), int(partition_tokens), _ptr(workspace), ws_bytes,
         _stream(stream))
     _check("paged_attention_decode", st)
+    return out
+
+
+def paged_attention_decode_append(out, q, key, value, k_cache, v_cache, block_tables,
+                                  context_lens, scale, partition_tokens=512, workspace=None,
+                                  stream=None):
+    """The decode step's KV write and decode attention in one call: the rows
+    key/value [S, Hkv, D] go to each sequence's position context_lens[s] - 1
+    (the slot its block table gives) in both pools, and out [S, Hq, D] is the
+    attention over all context_lens[s] positions, that one included."""
+    _need_cuda("paged_attention_decode_append", out, q, key, value, k_cache, v_cache,
+               block_tables, context_lens)
+    N, B, Hkv, D = _cache_dims(k_cache)
+    S, Hq, _ = (int(x) for x in q.shape)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    for t in (key, value):
+        if tuple(t.shape) != (S, Hkv, D) or t.dtype != k_cache.dtype or not t.is_contiguous():
+            raise ValueError("key/value must be contiguous [num_seqs, num_kv_heads, head_dim] "
+                             "of the cache dtype")
+    max_blocks = int(block_tables.shape[1])
+    need = paged_attention_workspace_bytes(S, Hq, D, max_blocks * B, partition_tokens)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().paged_attention_decode_append(
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(key), _ptr(value),
+        _ptr(k_cache), _ptr(v_cache), _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables),
+        max_blocks, _ptr(context_lens), S, Hq, Hkv, D, B, N, float(scale),
+        int(partition_tokens), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("paged_attention_decode_append", st)
     return out
 
 

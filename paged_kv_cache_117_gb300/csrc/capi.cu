@@ -211,14 +211,18 @@ pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_p
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_block_copy launch");
 }
 
-pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
-                                  const void *k_cache, const void *v_cache, pkv_dtype dtype,
-                                  const int32_t *block_tables, int max_blocks,
-                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
-                                  int num_kv_heads, int head_dim, int block_size,
-                                  int num_blocks, float scale, int partition_tokens,
-                                  void *workspace, size_t workspace_bytes,
-                                  pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Decode attention, optionally appending this step's token first (key_new /
+// value_new non-null).
+pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void *key_new,
+                       const void *value_new, void *k_cache, void *v_cache, pkv_dtype dtype,
+                       const int32_t *block_tables, int max_blocks, const int32_t *context_lens,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, int partition_tokens,
+                       void *workspace, size_t workspace_bytes, pkv_stream_t stream,
+                       const char *what) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks <= 0 || partition_tokens < 0)
     return PKV_ERR_RANGE;
@@ -262,6 +266,17 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
       overlap(workspace, need, block_tables, tab_sz) ||
       overlap(workspace, need, context_lens, (size_t)num_seqs * 4))
     return PKV_ERR_ALIAS;
+  if (key_new || value_new) {
+    if (!key_new || !value_new) return PKV_ERR_NULL;
+    if (!aligned(key_new, 16) || !aligned(value_new, 16)) return PKV_ERR_ALIGN;
+    // the new rows are read while the pools are written: no overlap with
+    // anything the call writes
+    const size_t row_sz = (size_t)num_seqs * num_kv_heads * head_dim * 2;
+    for (const void *r : {key_new, value_new})
+      if (overlap(r, row_sz, k_cache, pool) || overlap(r, row_sz, v_cache, pool) ||
+          overlap(r, row_sz, out, out_sz) || overlap(r, row_sz, workspace, need))
+        return PKV_ERR_ALIAS;
+  }
 
   CUtensorMap kmap, vmap;
   const int rows16 = block_size < 16 ? block_size : 16;   // decode: up to 16 tokens a box
@@ -297,6 +312,10 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
   p.part_o = max_parts > 1 ? reinterpret_cast<float *>(ws + lay.part_o) : nullptr;
   p.part_ml = max_parts > 1 ? reinterpret_cast<float *>(ws + lay.part_ml) : nullptr;
   p.flags = flags;
+  p.key_new = key_new;
+  p.value_new = value_new;
+  p.k_pool = key_new ? k_cache : nullptr;
+  p.v_pool = key_new ? v_cache : nullptr;
 
   int launches = 0;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -304,7 +323,42 @@ pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
       dtype == PKV_BF16
           ? pkv::launch_decode_bf16(kmap, vmap, p, head_dim, block_size, st, &launches)
           : pkv::launch_decode_f16(kmap, vmap, p, head_dim, block_size, st, &launches);
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention_decode launch");
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, what);
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_attention_decode(void *out, pkv_dtype out_dtype, const void *q,
+                                  const void *k_cache, const void *v_cache, pkv_dtype dtype,
+                                  const int32_t *block_tables, int max_blocks,
+                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int num_blocks, float scale, int partition_tokens,
+                                  void *workspace, size_t workspace_bytes,
+                                  pkv_stream_t stream) {
+  // the pools are only read when nothing is appended
+  return decode_impl(out, out_dtype, q, nullptr, nullptr, const_cast<void *>(k_cache),
+                     const_cast<void *>(v_cache), dtype, block_tables, max_blocks,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, partition_tokens, workspace, workspace_bytes, stream,
+                     "paged_attention_decode launch");
+}
+
+pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const void *q,
+                                         const void *key, const void *value, void *k_cache,
+                                         void *v_cache, pkv_dtype dtype,
+                                         const int32_t *block_tables, int max_blocks,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int num_blocks, float scale,
+                                         int partition_tokens, void *workspace,
+                                         size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs > 0 && (!key || !value)) return PKV_ERR_NULL;
+  return decode_impl(out, out_dtype, q, key, value, k_cache, v_cache, dtype, block_tables,
+                     max_blocks, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, workspace, workspace_bytes,
+                     stream, "paged_attention_decode_append launch");
 }
 
 pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q,

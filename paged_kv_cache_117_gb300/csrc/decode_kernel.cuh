@@ -192,6 +192,7 @@ struct WarpLoads {
   int part;         // partition
   int hc;           // KV head x query-head chunk index
   int L;            // context length (clamped)
+  bool append;      // position L - 1 comes from the step's new K/V rows
   int kvh;          // KV head
   int j0;           // first block of this warp
   int n_w;          // blocks of this warp
@@ -209,7 +210,8 @@ __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodePar
   const int2 item = __ldcg(p.items + unit / HC);
   const int hc = (int)(unit % HC);
   const int s = item.x, part = item.y;
-  const int L = clamp_len(__ldg(p.context_lens + s), p.max_blocks * B);
+  const int L0 = __ldg(p.context_lens + s);
+  const int L = clamp_len(L0, p.max_blocks * B);
   const int nb = (L + B - 1) / B;
   const int jb = part * p.part_blocks;
   const int je = min(nb, jb + p.part_blocks);
@@ -217,6 +219,7 @@ __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodePar
   wl.part = part;
   wl.hc = hc;
   wl.L = L;
+  wl.append = p.key_new != nullptr && L0 >= 1 && L0 == L;
   wl.kvh = hc / p.num_gchunks;
   wl.j0 = jb + w;
   wl.n_w = wl.j0 < je ? (je - wl.j0 + NW - 1) / NW : 0;
@@ -379,6 +382,19 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
     const int hq0 = kvh * p.group + g0;
     const size_t out_base = ((size_t)s * p.num_q_heads + hq0) * D;
 
+    // Appending: the warp whose blocks include position L - 1 fetches this
+    // step's K (lanes 0..D/8-1) or V (the next D/8 lanes) row piece now, so
+    // the load is long done when that chunk comes up.
+    constexpr int PIECES = D / 8;              // 16-byte pieces of one row
+    const bool app_warp = cur.append && cur.n_w > 0 && cur.j0 + (cur.n_w - 1) * NW == nb - 1;
+    uint4 app_val = make_uint4(0u, 0u, 0u, 0u);
+    if (app_warp && lane < 2 * PIECES) {
+      const bool isv = lane >= PIECES;
+      const T *src = static_cast<const T *>(isv ? p.value_new : p.key_new) +
+                     ((size_t)s * p.num_kv_heads + kvh) * D;
+      app_val = __ldg(reinterpret_cast<const uint4 *>(src) + (isv ? lane - PIECES : lane));
+    }
+
     // softmax state of heads 8nh + cq + {0, 1}
     float mr[NH][2], lr[NH][2];
     float o[NH][C::MT][4];
@@ -420,6 +436,32 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (app_warp && j * B + c * C::CH + valid == L) {
+        // this step's token (position L - 1, row valid - 1 of the chunk): its
+        // K and V rows come from the step's inputs, whatever the slot holds,
+        // and the unit of query-head chunk 0 stores them in the pool.  No
+        // unit of this call takes that slot's bytes from the pool.
+        const int row = valid - 1;
+        if (lane < 2 * PIECES) {
+          const bool isv = lane >= PIECES;
+          const int pc = isv ? lane - PIECES : lane;
+          const int sb = pc >> 3, ch = pc & 7;
+          const uint4 val = app_val;
+          unsigned char *base = smem + ((isv ? vb : kb) - stage_smem);
+          *reinterpret_cast<uint4 *>(base + sb * C::SUB_BYTES + row * 128 + ((ch ^ (row & 7)) << 4)) =
+              val;
+          if (gc == 0) {
+            const int pb = __ldg(cur.trow + j);
+            if ((unsigned)pb < (unsigned)p.num_blocks) {   // a bad id was flagged at load
+              const size_t dst = (((size_t)pb * B + (L - 1) % B) * p.num_kv_heads + kvh) * D;
+              reinterpret_cast<uint4 *>(static_cast<T *>(isv ? p.v_pool : p.k_pool) + dst)[pc] =
+                  val;
+            }
+          }
+        }
+        fence_proxy_async_smem();   // before a later TMA load refills this stage
         __syncwarp();
       }
 

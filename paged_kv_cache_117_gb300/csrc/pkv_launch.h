@@ -66,6 +66,12 @@ struct DecodeParams {
   unsigned *seq_done;            // [S, num_hc] partitions finished per sequence
   int2 *items;                   // [S * max_parts] (sequence, partition) work list
   unsigned *flags;               // device flag word
+  // Appending this step's token (null: the pool already holds it): its K and V
+  // rows [S, Hkv, D], used for position L - 1 and stored into the pools.
+  const void *key_new = nullptr;
+  const void *value_new = nullptr;
+  void *k_pool = nullptr;
+  void *v_pool = nullptr;
 };
 
 // Launch the work-list pass and the decode pass for one cache dtype /

@@ -131,21 +131,31 @@ def oracle_step(plan: StepPlan, k_pool_cpu_blocks, v_pool_cpu_blocks, block_ids,
 
 
 def run_gpu_step(plan: StepPlan, k_cache, v_cache, q, key, value, out_dtype=torch.float32,
-                 partition_tokens=None, run_setup=True):
+                 partition_tokens=None, run_setup=True, append=False):
     """Setup copies (if any), then the step: copy -> write -> attend, through
-    the library.  Returns out (device tensor)."""
+    the library (``append``: copy -> paged_attention_decode_append, the write
+    and the attention in one call).  Returns out (device tensor)."""
     import paged_kv_cache_117_gb300 as pkv
     dev = k_cache.device
     if run_setup and plan.setup_pairs:
         pkv.paged_block_copy(k_cache, v_cache, pairs_tensor(plan.setup_pairs).to(dev))
     pkv.paged_block_copy(k_cache, v_cache, pairs_tensor(plan.step_pairs).to(dev))
-    slots = torch.tensor(plan.slots, dtype=torch.int64, device=dev)
-    pkv.paged_kv_write(key, value, k_cache, v_cache, slots)
     tables = table_tensor(plan).to(dev)
     lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
     S = len(plan.lens)
     out = torch.empty((S, plan.w.num_q_heads, plan.w.head_dim), dtype=out_dtype, device=dev)
     pt = plan.w.partition_tokens if partition_tokens is None else partition_tokens
+    if append:
+        # the slot the call derives (position L - 1) is the manager's slot
+        B = plan.w.block_size
+        for s, slot in enumerate(plan.slots):
+            L = plan.lens[s]
+            assert slot == (plan.tables[s][(L - 1) // B] * B + (L - 1) % B if L else -1)
+        pkv.paged_attention_decode_append(out, q, key, value, k_cache, v_cache, tables, lens,
+                                          plan.w.scale, partition_tokens=pt)
+        return out
+    slots = torch.tensor(plan.slots, dtype=torch.int64, device=dev)
+    pkv.paged_kv_write(key, value, k_cache, v_cache, slots)
     pkv.paged_attention_decode(out, q, k_cache, v_cache, tables, lens, plan.w.scale,
                                partition_tokens=pt)
     return out

@@ -100,6 +100,32 @@ def test_decode_validation(lib):
     assert decode(lib, S=0) == OK           # nothing to do: returns before any CUDA call
 
 
+def append(lib, **kw):
+    a = dict(out=fake(0), out_dt=F32, q=fake(1), key=fake(7), val=fake(8), k=fake(2), v=fake(3),
+             dt=BF16, tab=fake(4), max_blocks=4, lens=fake(5), S=2, Hq=8, Hkv=2, D=128, B=16,
+             N=8, scale=0.1, pt=0, ws=fake(6), ws_bytes=1 << 20)
+    a.update(kw)
+    return lib.paged_attention_decode_append(
+        a["out"], a["out_dt"], a["q"], a["key"], a["val"], a["k"], a["v"], a["dt"], a["tab"],
+        a["max_blocks"], a["lens"], a["S"], a["Hq"], a["Hkv"], a["D"], a["B"], a["N"],
+        a["scale"], a["pt"], a["ws"], a["ws_bytes"], None)
+
+
+def test_decode_append_validation(lib):
+    assert append(lib, key=None) == NULL
+    assert append(lib, val=None) == NULL
+    assert append(lib, q=None) == NULL
+    assert append(lib, key=fake(7) + 8) == ALIGN
+    assert append(lib, key=fake(2) + 256) == ALIAS          # inside the K pool
+    assert append(lib, val=fake(3)) == ALIAS                # the V pool itself
+    assert append(lib, key=fake(0) + 64) == ALIAS           # the output
+    assert append(lib, val=fake(6) + 512) == ALIAS          # the workspace
+    assert append(lib, D=96) == SHAPE
+    assert append(lib, ws=None) == WS
+    assert append(lib, S=0) == OK
+    assert append(lib, S=0, key=None, val=None) == OK       # nothing to append or read
+
+
 def chunked(lib, **kw):
     a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
              max_blocks=4, lens=fake(5), qs=fake(6), S=2, T=64, maxq=32, Hq=8, Hkv=2, D=128,

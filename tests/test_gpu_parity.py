@@ -34,10 +34,17 @@ def _flags():
 
 
 def run_full_compare(w, out_dtype=torch.float32, partition_tokens=None, width=None,
-                     poison_tail=False):
-    """Whole step on both sides; the full pool and every output compared."""
+                     poison_tail=False, append=False, poison_new_slot=False):
+    """Whole step on both sides; the full pool and every output compared.
+    ``append``: the GPU side writes and attends in one call.
+    ``poison_new_slot``: each sequence's new slot holds NaN before the step."""
     plan = gh.plan_step(w, width=width)
     k, v = wl.make_pool(w, "cpu")
+    if poison_new_slot:
+        for slot in plan.slots:
+            if slot >= 0:
+                k[slot // w.block_size, slot % w.block_size] = float("nan")
+                v[slot // w.block_size, slot % w.block_size] = float("nan")
     if poison_tail:
         # unused slots of every last block hold NaN / Inf bit patterns
         for s, t in enumerate(plan.tables):
@@ -50,7 +57,7 @@ def run_full_compare(w, out_dtype=torch.float32, partition_tokens=None, width=No
     ref = gh.oracle_step(plan, k, v, ids, q, key, value, range(w.num_seqs))
     kd, vd = k.cuda(), v.cuda()
     out = gh.run_gpu_step(plan, kd, vd, q.cuda(), key.cuda(), value.cuda(), out_dtype,
-                          partition_tokens)
+                          partition_tokens, append=append)
     torch.cuda.synchronize()
     assert _flags() == 0
     kg, vg = kd.cpu(), vd.cpu()
