@@ -4,7 +4,11 @@
 One step = one pass of the whole path over one batch: the batched
 copy-on-write block copy (when the workload has copies), the KV write of every
 sequence's new token, and decode attention (partitioned pass + merge) -- all
-through the library's C ABI.  Inputs are resident in HBM when timing starts;
+through the library's C ABI; by default the write happens inside the
+attention call (paged_attention_decode_append; --kv-write separate runs
+paged_kv_write then paged_attention_decode).  Inputs are resident in HBM when
+timing starts.  Before each timed loop the GPU spins ~50 ms (outside every
+timed span, inside wall_s_timed) so that the host queues steps ahead of it.
 L2 is flushed before every timed step, outside the timed span: a 256 MiB
 buffer is written (evicting what the last step left in L2), then another
 256 MiB buffer is read, so that the flush's own dirty lines are written back
@@ -60,6 +64,15 @@ class L2Flush:
     def __call__(self):
         self.w.zero_()
         self.sink.add_(self.r.sum())
+
+
+def host_head_start():
+    """Gives the host a head start before a timed loop: the GPU first spins
+    for ~50 ms (a fixed cycle count), outside every timed span, while the
+    host queues the steps, so that a pause of the host (a page fault, a
+    collector pass) does not leave the GPU idle inside a step's span."""
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(100_000_000)
 
 
 def parse_args():
@@ -577,6 +590,7 @@ def run_native(a, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    host_head_start()
     for s0, s1, d0, d1 in evs:
         flush()
         s0.record(stream)
@@ -591,6 +605,7 @@ def run_native(a, world, rank, local):
     clocks = sampler.stop()
     step_ms = sum(s0.elapsed_time(s1) for s0, s1, _, _ in evs) / K
     if graph is not None:   # layer 0's attention call, timed eagerly for the roofline
+        host_head_start()
         for _, _, d0, d1 in evs:
             flush()
             d0.record(stream)
@@ -638,6 +653,7 @@ def run_native(a, world, rank, local):
     e2e_evs = [(ev(), ev()) for _ in range(K if e2e_step else 0)]
     barrier(world)
     torch.cuda.synchronize()
+    host_head_start()
     for e0, e1 in e2e_evs:
         flush()
         e0.record(stream)
@@ -791,6 +807,7 @@ def run_native_chunked(a, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    host_head_start()
     for s0, s1, d0, d1 in evs:
         flush()
         s0.record(stream)
@@ -830,6 +847,7 @@ def run_native_chunked(a, world, rank, local):
     e2e_evs = [(ev(), ev()) for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
+    host_head_start()
     for e0, e1 in e2e_evs:
         flush()
         e0.record(stream)
