@@ -52,7 +52,7 @@ struct DecodeParams {
   int num_q_heads;
   int num_kv_heads;
   int group;                     // Hq / Hkv
-  int num_gchunks;               // query-head chunks (<= 8 heads) per KV head
+  int num_gchunks;               // query-head chunks (<= 16 heads each) per KV head
   int num_hc;                    // num_kv_heads * num_gchunks
   int head_dim;
   int block_size;
