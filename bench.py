@@ -300,11 +300,17 @@ CHUNKED_SOURCES = ("paged_kv_cache_117_gb300/csrc/chunked_kernel.cuh",
 
 
 def sources_sha256(sources):
+    """Hash of the kernel's sources with comments and whitespace removed, so
+    that a comment edit does not invalidate a profile of unchanged code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in sources:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 
