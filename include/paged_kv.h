@@ -81,6 +81,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 #define PKV_FLAG_LEN_RANGE 0x8u   /* a context length was < 0 or > max_blocks * block_size */
 #define PKV_FLAG_TIMEOUT 0x10u    /* a kernel gave up waiting on its own tile loads */
 #define PKV_FLAG_V_RANGE 0x20u    /* PKV_P_F16 met a bf16 V value beyond the f16 range (clamped) */
+#define PKV_FLAG_PAIR_CONFLICT 0x40u /* a copy pair's dst was another pair's dst or src (skipped) */
 
 /*
  * paged_kv_write -- store new keys/values into their slots.
@@ -116,9 +117,11 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache,
  *
  *   block_pairs  int64 [num_pairs][2] = (src, dst), DEVICE memory.
  *
- * Preconditions (the block manager's invariants; not checked on the host
- * because the pairs live on the device): every dst appears once and no dst is
- * also a src in the same call.  A pair naming a block outside [0, num_blocks)
+ * Preconditions (the block manager's invariants): every dst appears once and
+ * no dst is also a src in the same call.  The pairs live on the device, so
+ * the kernel checks them: a pair whose dst is another pair's dst or src is
+ * skipped and flagged (PKV_FLAG_PAIR_CONFLICT) -- the copies of one call run
+ * in no particular order -- and a pair naming a block outside [0, num_blocks)
  * is skipped and flagged (PKV_FLAG_PAIR_RANGE).  num_pairs == 0 is a no-op.
  */
 pkv_status paged_block_copy(void *k_cache, void *v_cache,

@@ -25,6 +25,7 @@ FLAG_PAIR_RANGE = 0x4
 FLAG_LEN_RANGE = 0x8
 FLAG_TIMEOUT = 0x10
 FLAG_V_RANGE = 0x20
+FLAG_PAIR_CONFLICT = 0x40
 
 EXPORTED_SYMBOLS = (
     "paged_kv_write",

@@ -28,6 +28,21 @@ __global__ void __launch_bounds__(COPY_THREADS)
     if (chunk == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(flags, PKV_FLAG_PAIR_RANGE);
     return;
   }
+  // The copies of one call run in any order, so a pair whose dst is also
+  // another pair's dst or src would race: such a pair is skipped and flagged
+  // (the block manager never produces one).
+  bool clash = false;
+  for (int i = threadIdx.x; i < num_pairs; i += COPY_THREADS) {
+    if (i == pair) continue;
+    const long long si = __ldg(reinterpret_cast<const long long *>(pairs) + 2 * i);
+    const long long di = __ldg(reinterpret_cast<const long long *>(pairs) + 2 * i + 1);
+    clash |= si == dst || di == dst;
+  }
+  if (__syncthreads_or(clash)) {
+    if (chunk == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+      atomicOr(flags, PKV_FLAG_PAIR_CONFLICT);
+    return;
+  }
   uint4 *pool = blockIdx.y == 0 ? k_cache : v_cache;
   const uint4 *s = pool + src * block_vecs;
   uint4 *d = pool + dst * block_vecs;

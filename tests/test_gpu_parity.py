@@ -231,6 +231,28 @@ def test_copy_bitexact_whole_pool(b, d):
     assert _flags() == 0
 
 
+def test_conflicting_copy_pairs_are_skipped_and_flagged():
+    """Copies of one call run in no order: pairs whose dst repeats another
+    pair's dst, or is another pair's src, are skipped and flagged; the other
+    pairs are copied (compared with the oracle copying only those)."""
+    import oracle.paged_ops as ops
+    import paged_kv_cache_117_gb300 as pkv
+    g = torch.Generator().manual_seed(11)
+    N, B, H, D = 64, 16, 2, 128
+    k = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    pairs = [(1, 10), (2, 11), (3, 10),      # dst 10 twice: both skipped
+             (4, 12), (12, 13),              # 12 is a dst and a src: (4, 12) skipped
+             (5, 20), (6, 21)]               # clean
+    kr, vr = k.clone(), v.clone()
+    ops.copy_blocks(kr, vr, [(2, 11), (12, 13), (5, 20), (6, 21)])
+    kd, vd = k.cuda(), v.cuda()
+    pkv.paged_block_copy(kd, vd, gh.pairs_tensor(pairs).cuda())
+    torch.cuda.synchronize()
+    assert _flags() == pkv.FLAG_PAIR_CONFLICT
+    assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr)
+
+
 def test_empty_calls_launch_nothing():
     import paged_kv_cache_117_gb300 as pkv
     k = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
