@@ -23,7 +23,6 @@ on a bounded sample of the same workload instead.
 """
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess

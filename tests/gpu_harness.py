@@ -8,7 +8,6 @@ copies of the same inputs -- taken before any library kernel touches them.
 """
 from __future__ import annotations
 
-import math
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 

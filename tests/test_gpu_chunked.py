@@ -3,7 +3,6 @@ the oracle: the chunk's K/V rows written through paged_kv_write, then
 paged_attention_chunked, every output row compared (fp32 output within 2e-3;
 16-bit outputs within max(2e-3, 1 ulp) of the rounded oracle) and the pool
 compared bit-exactly."""
-import math
 
 import pytest
 import torch

@@ -4,7 +4,6 @@ Bit-exact for the KV write and the block copy (whole pool compared);
 attention within 2e-3 max abs error for fp32 outputs, and within
 max(2e-3, 1 ulp) of the once-rounded oracle for 16-bit outputs.
 """
-import dataclasses
 import random
 
 import pytest

@@ -1,7 +1,6 @@
 """The oracle's multi-query (chunked) attention against its pins, and planted
 mistakes that the pins must catch."""
 import pytest
-import torch
 
 import oracle.paged_ops as ops
 from tests import chunked_checks as cc
