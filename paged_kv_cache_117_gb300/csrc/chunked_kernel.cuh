@@ -325,27 +325,34 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // P_B(j) V(j), S_B(j+1).
     constexpr uint32_t ID_S = tc::idesc_f16(BF16, CK_ROWS, CK_BN, false);
     constexpr uint32_t ID_PV = tc::idesc_f16(BF16 && !P16, CK_ROWS, D, true);
+    // The MMA issue rate is set by this one thread, and an MMA whose
+    // descriptors are rebuilt from addresses just before it issues well below
+    // the pipe's rate (measured on this GPU: ~100 cycles apart instead of 66
+    // for a 128 x 128 x 16 MMA).  So a tile's descriptors are built once and
+    // advanced by adding each K step's offset in 16-byte units to the
+    // start-address field (no carry: shared-memory addresses stay below 2^18).
     auto issue_s = [&](int x, int j) {           // S_x(j); K(j) has landed
       if (lane == 0) {
-        const uint32_t qa = sb + C::OFF_Q + x * C::Q_BYTES;
-        const uint32_t ka = sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES;
+        const uint64_t dq = tc::sdesc_sw128(sb + C::OFF_Q + x * C::Q_BYTES, 16, 1024);
+        const uint64_t dk = tc::sdesc_sw128(sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES, 16, 1024);
+        const uint32_t d = tmem + (uint32_t)x * C::TILE_COLS;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (uint32_t)(k >> 2) * C::HALF + (uint32_t)(k & 3) * 32u;
-          tc::mma_f16_ss(tmem + (uint32_t)x * C::TILE_COLS, tc::sdesc_sw128(qa + off, 16, 1024),
-                         tc::sdesc_sw128(ka + off, 16, 1024), ID_S, k > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((k >> 2) * C::HALF + (k & 3) * 32) >> 4);
+          tc::mma_f16_ss(d, dq + off, dk + off, ID_S, k > 0 ? 1u : 0u);
         }
         tc::commit(bar(CB_SF + x));
       }
     };
     auto issue_pv = [&](int x, int j) {          // O_x += P_x(j) V(j)
       if (lane == 0) {
-        const uint32_t va = sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES;
+        const uint64_t dv = tc::sdesc_sw128(sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
         const uint32_t t0 = tmem + (uint32_t)x * C::TILE_COLS;
+        const uint32_t first = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int k = 0; k < CK_BN / 16; ++k) {
-          const uint64_t bv = tc::sdesc_sw128(va + (uint32_t)k * 2048u, C::HALF, 1024);
-          tc::mma_f16_ts(t0 + C::COL_O, t0 + 8u * k, bv, ID_PV, (j > 0 || k > 0) ? 1u : 0u);
+          const uint64_t bv = dv + (uint64_t)(k * (2048 >> 4));   // 16 V rows per K step
+          tc::mma_f16_ts(t0 + C::COL_O, t0 + 8u * k, bv, ID_PV, k > 0 ? 1u : first);
           if (!P16) tc::mma_f16_ts(t0 + C::COL_O, t0 + C::COL_PL + 8u * k, bv, ID_PV, 1u);
         }
         if (j == nk[x] - 1) tc::commit(bar(CB_OF + x));
