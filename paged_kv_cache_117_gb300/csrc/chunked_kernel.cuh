@@ -330,16 +330,20 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // the pipe's rate (measured on this GPU: ~100 cycles apart instead of 66
     // for a 128 x 128 x 16 MMA).  So a tile's descriptors are built once and
     // advanced by adding each K step's offset in 16-byte units to the
-    // start-address field (no carry: shared-memory addresses stay below 2^18).
+    // start-address field of the low word (no carry: shared-memory addresses
+    // stay below 2^18), the high word passed through unchanged.
     auto issue_s = [&](int x, int j) {           // S_x(j); K(j) has landed
       if (lane == 0) {
         const uint64_t dq = tc::sdesc_sw128(sb + C::OFF_Q + x * C::Q_BYTES, 16, 1024);
         const uint64_t dk = tc::sdesc_sw128(sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES, 16, 1024);
         const uint32_t d = tmem + (uint32_t)x * C::TILE_COLS;
+        const uint32_t hq = (uint32_t)(dq >> 32), hk = (uint32_t)(dk >> 32);
+        const uint32_t lq = (uint32_t)dq, lk = (uint32_t)dk;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t off = (uint64_t)(((k >> 2) * C::HALF + (k & 3) * 32) >> 4);
-          tc::mma_f16_ss(d, dq + off, dk + off, ID_S, k > 0 ? 1u : 0u);
+          const uint32_t off = (uint32_t)(((k >> 2) * C::HALF + (k & 3) * 32) >> 4);
+          tc::mma_f16_ss(d, tc::desc_pack(lq + off, hq), tc::desc_pack(lk + off, hk), ID_S,
+                         k > 0 ? 1u : 0u);
         }
         tc::commit(bar(CB_SF + x));
       }
@@ -349,9 +353,10 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
         const uint64_t dv = tc::sdesc_sw128(sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
         const uint32_t t0 = tmem + (uint32_t)x * C::TILE_COLS;
         const uint32_t first = j > 0 ? 1u : 0u;
+        const uint32_t hv = (uint32_t)(dv >> 32), lv = (uint32_t)dv;
 #pragma unroll
         for (int k = 0; k < CK_BN / 16; ++k) {
-          const uint64_t bv = dv + (uint64_t)(k * (2048 >> 4));   // 16 V rows per K step
+          const uint64_t bv = tc::desc_pack(lv + (uint32_t)(k * (2048 >> 4)), hv);   // 16 V rows a step
           tc::mma_f16_ts(t0 + C::COL_O, t0 + 8u * k, bv, ID_PV, k > 0 ? 1u : first);
           if (!P16) tc::mma_f16_ts(t0 + C::COL_O, t0 + C::COL_PL + 8u * k, bv, ID_PV, 1u);
         }

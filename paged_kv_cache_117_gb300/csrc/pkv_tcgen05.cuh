@@ -61,6 +61,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor from its two 32-bit words (low: start address and leading
+// offset; high: stride offset, version, swizzle).
+__device__ __forceinline__ uint64_t desc_pack(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 // Instruction descriptor of a dense kind::f16 MMA with an fp32 accumulator:
 // A and B both bf16 (or both f16), A K-major, B K-major or MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int m, int n, bool b_mn_major) {
