@@ -332,28 +332,36 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // advanced by adding each K step's offset in 16-byte units to the
     // start-address field of the low word (no carry: shared-memory addresses
     // stay below 2^18), the high word passed through unchanged.
-    auto issue_s = [&](int x, int j) {           // S_x(j); K(j) has landed
+    // High words are the same for every tile; low words of the Q tiles are
+    // fixed; a K or V stage's low word is computed before the waits that
+    // precede its MMAs.
+    const uint32_t hqk = (uint32_t)(tc::sdesc_sw128(sb, 16, 1024) >> 32);
+    const uint32_t hv = (uint32_t)(tc::sdesc_sw128(sb, C::HALF, 1024) >> 32);
+    const uint32_t lq[2] = {(uint32_t)tc::sdesc_sw128(sb + C::OFF_Q, 16, 1024),
+                            (uint32_t)tc::sdesc_sw128(sb + C::OFF_Q + C::Q_BYTES, 16, 1024)};
+    auto k_lo = [&](int j) {                     // low word of K(j)'s stage
+      return (uint32_t)tc::sdesc_sw128(sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES, 16, 1024);
+    };
+    auto v_lo = [&](int j) {
+      return (uint32_t)tc::sdesc_sw128(sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
+    };
+    auto issue_s = [&](int x, uint32_t lk) {     // S_x = Q_x K^T, K's stage low word lk
       if (lane == 0) {
-        const uint64_t dq = tc::sdesc_sw128(sb + C::OFF_Q + x * C::Q_BYTES, 16, 1024);
-        const uint64_t dk = tc::sdesc_sw128(sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES, 16, 1024);
         const uint32_t d = tmem + (uint32_t)x * C::TILE_COLS;
-        const uint32_t hq = (uint32_t)(dq >> 32), hk = (uint32_t)(dk >> 32);
-        const uint32_t lq = (uint32_t)dq, lk = (uint32_t)dk;
+        const uint32_t lqx = x ? lq[1] : lq[0];
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (uint32_t)(((k >> 2) * C::HALF + (k & 3) * 32) >> 4);
-          tc::mma_f16_ss(d, tc::desc_pack(lq + off, hq), tc::desc_pack(lk + off, hk), ID_S,
+          tc::mma_f16_ss(d, tc::desc_pack(lqx + off, hqk), tc::desc_pack(lk + off, hqk), ID_S,
                          k > 0 ? 1u : 0u);
         }
         tc::commit(bar(CB_SF + x));
       }
     };
-    auto issue_pv = [&](int x, int j) {          // O_x += P_x(j) V(j)
+    auto issue_pv = [&](int x, int j, uint32_t lv) {   // O_x += P_x(j) V(j), V's low word lv
       if (lane == 0) {
-        const uint64_t dv = tc::sdesc_sw128(sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
         const uint32_t t0 = tmem + (uint32_t)x * C::TILE_COLS;
         const uint32_t first = j > 0 ? 1u : 0u;
-        const uint32_t hv = (uint32_t)(dv >> 32), lv = (uint32_t)dv;
 #pragma unroll
         for (int k = 0; k < CK_BN / 16; ++k) {
           const uint64_t bv = tc::desc_pack(lv + (uint32_t)(k * (2048 >> 4)), hv);   // 16 V rows a step
@@ -370,12 +378,13 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     ok = warp_wait(bar(CB_Q), 0) && wait_k(0);
     if (ok) {
       tc::fence_after_sync();
-      issue_s(0, 0);
-      if (nk[1] > 0) issue_s(1, 0);
+      issue_s(0, k_lo(0));
+      if (nk[1] > 0) issue_s(1, k_lo(0));
       if (lane == 0) tc::commit(bar(CB_KE + 0));
       __syncwarp();
     }
     for (int j = 0; j < nkv && ok; ++j) {
+      const uint32_t lv = v_lo(j), lk1 = k_lo(j + 1);   // before the waits
       if (!warp_wait(bar((CONVERT ? CB_VC : CB_VF) + j % CK_VST), (uint32_t)(j / CK_VST) & 1u) ||
           !warp_wait(bar(CB_PF + 0), (uint32_t)j & 1u)) {
         ok = false;
@@ -395,21 +404,21 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
         __syncwarp();
       }
       tc::fence_after_sync();
-      issue_pv(0, j);
+      issue_pv(0, j, lv);
       if (j + 1 < nk[0]) {
         if (!wait_k(j + 1)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_s(0, j + 1);
+        issue_s(0, lk1);
         if (j + 1 >= nk[1] && lane == 0) tc::commit(bar(CB_KE + (j + 1) % CK_KST));
       }
       if (j < nk[1]) {
         if (!warp_wait(bar(CB_PF + 1), (uint32_t)j & 1u)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_pv(1, j);
+        issue_pv(1, j, lv);
       }
       if (lane == 0) tc::commit(bar(CB_VE + j % CK_VST));
       if (j + 1 < nk[1]) {
-        issue_s(1, j + 1);
+        issue_s(1, lk1);
         if (lane == 0) tc::commit(bar(CB_KE + (j + 1) % CK_KST));
       }
       __syncwarp();
