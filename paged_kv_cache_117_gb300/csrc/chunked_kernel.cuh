@@ -328,13 +328,12 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // The MMA issue rate is set by this one thread, and an MMA whose
     // descriptors are rebuilt from addresses just before it issues well below
     // the pipe's rate (measured on this GPU: ~100 cycles apart instead of 66
-    // for a 128 x 128 x 16 MMA).  So a tile's descriptors are built once and
-    // advanced by adding each K step's offset in 16-byte units to the
-    // start-address field of the low word (no carry: shared-memory addresses
-    // stay below 2^18), the high word passed through unchanged.
-    // High words are the same for every tile; low words of the Q tiles are
-    // fixed; a K or V stage's low word is computed before the waits that
-    // precede its MMAs.
+    // for a 128 x 128 x 16 MMA).  So the descriptors' high words (stride,
+    // version, swizzle: the same for every tile) and the Q tiles' low words
+    // are built once, a K or V stage's low word before the barrier waits that
+    // precede its MMAs, and each K step adds its offset in 16-byte units to
+    // the low word's start-address field (no carry: shared-memory addresses
+    // stay below 2^18).
     const uint32_t hqk = (uint32_t)(tc::sdesc_sw128(sb, 16, 1024) >> 32);
     const uint32_t hv = (uint32_t)(tc::sdesc_sw128(sb, C::HALF, 1024) >> 32);
     const uint32_t lq[2] = {(uint32_t)tc::sdesc_sw128(sb + C::OFF_Q, 16, 1024),
