@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(CB_SF + x), 1);
-      mbar_init(bar(CB_PF + x), 8);
+      mbar_init(bar(CB_PF + x), CONVERT ? 8 : 4);   // softmax warps writing P_x
       mbar_init(bar(CB_OF + x), 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(CB_PAIR + i), 64);
@@ -470,7 +470,124 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Per KV tile j: tile A, then tile B (when it needs tile j).
+    if constexpr (!CONVERT) {
+    // Warpgroup x owns query tile x: thread t holds row t (TMEM lane t) of it,
+    // all CK_BN key columns, so a row's maximum and sum need no exchange and
+    // the two tiles' softmax run side by side.
+    const int x = warp >> 2;                  // query tile of this warpgroup
+    const int r = tid & (CK_ROWS - 1);        // query row = TMEM lane
+    const int tl = r / G, g = r % G;
+    const uint32_t tt = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)x * C::TILE_COLS;
+    const float sl2 = p.scale_log2;
+    const int tok = tb[x] + tl;
+    const bool valid = x < ntile && tl < TQ && tok < te[x];
+    const int p_row = valid ? (L - n + tok) : pm[x];
+    float m = -INFINITY, l = 0.f;
+    uint32_t sr[CK_BN];
+    const int njx = x < ntile ? nk[x] : 0;
+    for (int j = 0; j < njx && ok; ++j) {
+      if (!warp_wait(bar(CB_SF + x), (uint32_t)j & 1u)) { ok = false; break; }
+      tc::fence_after_sync();
+      const int lim = p_row - j * CK_BN;      // columns 0..lim are visible
+      float alpha = 1.f;
+      bool resc = false;
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      {
+        // S all in registers, so P may overwrite its columns as it goes
+#pragma unroll
+        for (int c = 0; c < CK_BN / 32; ++c) tc::ld_32x32b_x32(tt + (uint32_t)(c * 32), sr + 32 * c);
+        tc::wait_ld();
+        if (lim < CK_BN - 1) {
+#pragma unroll
+          for (int c = 0; c < CK_BN; ++c)
+            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < CK_BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // running maximum in the exp2 domain, raised lazily
+        const float mnew = fmaxf(m, mx * sl2);
+        resc = mnew > m + CK_SLACK;
+        if (resc) {
+          alpha = fast_exp2(m - mnew);
+          m = mnew;
+        }
+        // P = exp2(s * scale * log2 e - m), 32 keys at a time: hi + lo pairs
+        // of the cache dtype, or (P16) f16 pairs with the row sum taken over
+        // the rounded values (each output row is then an exact convex
+        // combination)
+        const float2 negm = make_float2(-m, -m);
+#pragma unroll
+        for (int c = 0; c < CK_BN / 32; ++c) {
+          uint32_t hiw[16], low[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k0 = 32 * c + 2 * e;
+            const float2 v = fma2(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+                                  sl2x2, negm);
+            const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+            if constexpr (P16) {
+              hiw[e] = Mma<__half>::pack(pe.x, pe.y);
+              const float2 hf = Widen<__half>::pair(hiw[e]);
+              lsum[e & 1] = make_float2(lsum[e & 1].x + hf.x, lsum[e & 1].y + hf.y);
+            } else {
+              lsum[e & 1] = make_float2(lsum[e & 1].x + pe.x, lsum[e & 1].y + pe.y);
+              hiw[e] = Mma<T>::pack(pe.x, pe.y);
+              const float2 hf = Widen<T>::pair(hiw[e]);
+              low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
+            }
+          }
+          tc::st_32x32b_x16(tt + (uint32_t)(16 * c), hiw);
+          if (!P16) tc::st_32x32b_x16(tt + C::COL_PL + (uint32_t)(16 * c), low);
+        }
+      }
+      l = l * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
+      // O_x is quiet: the P_x V before this S_x has completed
+      if (j > 0 && __any_sync(FULL_MASK, resc)) {
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint32_t ta = tt + C::COL_O + (uint32_t)(c * 32);
+          tc::ld_32x32b_x32(ta, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st_32x32b_x32(ta, o);
+        }
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(CB_PF + x));
+    }
+    // ---- epilogue: O_x / l_x
+    if (x < ntile && ok) {
+      if (!warp_wait(bar(CB_OF + x), 0)) {
+        ok = false;
+      } else {
+        tc::fence_after_sync();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t row = ((size_t)(q0 + (valid ? tok : 0)) * p.num_q_heads +
+                            (size_t)kvh * G + g) * (size_t)D;
+        uint32_t o[32];
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          tc::ld_32x32b_x32(tt + C::COL_O + (uint32_t)(c * 32), o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+          if (valid) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
+        }
+      }
+    }
+    } else {
+    // (f16 P with a converted bf16 V: the converting warps leave fewer
+    // registers, so the two warpgroups split each tile's key columns and
+    // take tile A, then tile B, agreeing on a row's maximum through shared
+    // memory.)
     constexpr int HC = CK_BN / 2;             // key columns per thread
     constexpr int HD = D / 2;                 // output columns per thread
     const int wg = warp >> 2;
@@ -593,6 +710,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
         if (valid[x]) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
       }
+    }
     }
     if (!ok && lane == 0) atomicOr(p.flags, PKV_FLAG_TIMEOUT);
   }
