@@ -384,8 +384,11 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     }
     for (int j = 0; j < nkv && ok; ++j) {
       const uint32_t lv = v_lo(j), lk1 = k_lo(j + 1);   // before the waits
+      // V(j), P_A(j) and K(j + 1) (usually long landed) are all waited for
+      // first, so that P_A(j) V(j) and S_A(j + 1) issue back to back
+      const bool next_a = j + 1 < nk[0];
       if (!warp_wait(bar((CONVERT ? CB_VC : CB_VF) + j % CK_VST), (uint32_t)(j / CK_VST) & 1u) ||
-          !warp_wait(bar(CB_PF + 0), (uint32_t)j & 1u)) {
+          !warp_wait(bar(CB_PF + 0), (uint32_t)j & 1u) || (next_a && !wait_k(j + 1))) {
         ok = false;
         break;
       }
@@ -404,9 +407,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       }
       tc::fence_after_sync();
       issue_pv(0, j, lv);
-      if (j + 1 < nk[0]) {
-        if (!wait_k(j + 1)) { ok = false; break; }
-        tc::fence_after_sync();
+      if (next_a) {
         issue_s(0, lk1);
         if (j + 1 >= nk[1] && lane == 0) tc::commit(bar(CB_KE + (j + 1) % CK_KST));
       }
