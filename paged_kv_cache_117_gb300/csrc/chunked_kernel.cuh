@@ -29,17 +29,21 @@
 // commit tracks every earlier MMA of its thread, so when S_x is seen
 // complete, the previous P_x V (and so O_x) is complete too.
 //
-// Warp roles (384 threads; 448 when V is converted): warps 0-7 are two softmax warpgroups; thread t of
-// warpgroup wg owns query row t % 128 (TMEM lane) and key columns wg*64 ..
-// wg*64+63 of every tile of both query tiles, the two threads of a row
-// agreeing on its maximum through shared memory once per tile.  Warp 8
-// issues the TMA loads (the two Q tiles once; K and V tiles through rings,
-// one box per block (all its tokens) and 64 dims, the block-table entries
-// fetched a group of 32 ahead).  Warp 9 allocates TMEM and issues the MMAs
-// (one lane).  Warps 10-13 convert V tiles to f16 when P goes in as f16 and
-// the cache is bf16 (otherwise warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is bounded and a
-// timeout sets PKV_FLAG_TIMEOUT, after which each role stops issuing and
-// drains what it has in flight before the CTA frees its TMEM and exits.
+// Warp roles (384 threads; 448 when V is converted): warps 0-7 are two
+// softmax warpgroups; warpgroup x owns query tile x, thread t of it query row
+// t % 128 (TMEM lane) with all 128 key columns, so the two tiles' softmax run
+// side by side.  (When V is converted, the four extra warps leave fewer
+// registers: there thread t of warpgroup wg owns key columns wg*64 ..
+// wg*64+63 of row t % 128 of both tiles, and the two threads of a row agree
+// on its maximum through shared memory.)  Warp 8 issues the TMA loads (the
+// two Q tiles once; K and V tiles through rings, one box per block (all its
+// tokens) and 64 dims, the block-table entries fetched a group of 32 ahead).
+// Warp 9 allocates TMEM and issues the MMAs (one lane).  Warps 10-13 convert
+// V tiles to f16 when P goes in as f16 and the cache is bf16 (otherwise
+// warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is
+// bounded and a timeout sets PKV_FLAG_TIMEOUT, after which each role stops
+// issuing and drains what it has in flight before the CTA frees its TMEM and
+// exits.
 //
 // Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, K 3 x 32 KiB, V
 // 2 x 32 KiB, in the 128-byte swizzled layout (rows of 64 elements); one CTA
@@ -80,7 +84,8 @@ struct ChunkCfg {
   static constexpr int OFF_BAR = OFF_V + CK_VST * KV_BYTES;
   static constexpr int NBAR = 24;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-  // row-max exchange between the two softmax warpgroups: [2 rounds][2][128]
+  // (V converted) row-maximum exchange of the two softmax warpgroups:
+  // [2 rounds][2][128]
   static constexpr int OFF_RED = OFF_TMEM + 16;
   static constexpr int SMEM = OFF_RED + 2 * 2 * CK_ROWS * 4;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -97,9 +102,9 @@ enum : int {
   CB_VF = CB_KE + CK_KST,    // V stage full [CK_VST] (tx)
   CB_VE = CB_VF + CK_VST,    // V stage free [CK_VST] (MMA commit)
   CB_SF = CB_VE + CK_VST,    // S_x computed [2: tiles A, B] (MMA commit)
-  CB_PF = CB_SF + 2,         // P_x written [2] (8 arrivals)
+  CB_PF = CB_SF + 2,         // P_x written [2] (one arrival per softmax warp writing P_x)
   CB_OF = CB_PF + 2,         // O_x final [2] (MMA commit)
-  CB_PAIR = CB_OF + 2,       // row-statistics exchange of warps w and w + 4 [4] (64 arrivals)
+  CB_PAIR = CB_OF + 2,       // (V converted) row-maximum exchange of warps w, w + 4 [4] (64 arrivals)
   CB_VC = CB_PAIR + 4,       // V stage converted to f16 [CK_VST] (one arrival per converting thread)
   CB_COUNT = CB_VC + CK_VST,
 };
@@ -472,61 +477,191 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   } else {
     // ------------------------------------------------------------ softmax
     if constexpr (!CONVERT) {
-    // Warpgroup x owns query tile x: thread t holds row t (TMEM lane t) of it,
-    // all CK_BN key columns, so a row's maximum and sum need no exchange and
-    // the two tiles' softmax run side by side.
-    const int x = warp >> 2;                  // query tile of this warpgroup
-    const int r = tid & (CK_ROWS - 1);        // query row = TMEM lane
-    const int tl = r / G, g = r % G;
-    const uint32_t tt = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)x * C::TILE_COLS;
-    const float sl2 = p.scale_log2;
-    const int tok = tb[x] + tl;
-    const bool valid = x < ntile && tl < TQ && tok < te[x];
-    const int p_row = valid ? (L - n + tok) : pm[x];
-    float m = -INFINITY, l = 0.f;
-    uint32_t sr[CK_BN];
-    const int njx = x < ntile ? nk[x] : 0;
-    for (int j = 0; j < njx && ok; ++j) {
-      if (!warp_wait(bar(CB_SF + x), (uint32_t)j & 1u)) { ok = false; break; }
-      tc::fence_after_sync();
-      const int lim = p_row - j * CK_BN;      // columns 0..lim are visible
-      float alpha = 1.f;
-      bool resc = false;
-      const float2 sl2x2 = make_float2(sl2, sl2);
-      float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      {
-        // S all in registers, so P may overwrite its columns as it goes
+      // Warpgroup x owns query tile x: thread t holds row t (TMEM lane t) of it,
+      // all CK_BN key columns, so a row's maximum and sum need no exchange and
+      // the two tiles' softmax run side by side.
+      const int x = warp >> 2;                  // query tile of this warpgroup
+      const int r = tid & (CK_ROWS - 1);        // query row = TMEM lane
+      const int tl = r / G, g = r % G;
+      const uint32_t tt = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)x * C::TILE_COLS;
+      const float sl2 = p.scale_log2;
+      const int tok = tb[x] + tl;
+      const bool valid = x < ntile && tl < TQ && tok < te[x];
+      const int p_row = valid ? (L - n + tok) : pm[x];
+      float m = -INFINITY, l = 0.f;
+      uint32_t sr[CK_BN];
+      const int njx = x < ntile ? nk[x] : 0;
+      for (int j = 0; j < njx && ok; ++j) {
+        if (!warp_wait(bar(CB_SF + x), (uint32_t)j & 1u)) { ok = false; break; }
+        tc::fence_after_sync();
+        const int lim = p_row - j * CK_BN;      // columns 0..lim are visible
+        float alpha = 1.f;
+        bool resc = false;
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        {
+          // S all in registers, so P may overwrite its columns as it goes
 #pragma unroll
-        for (int c = 0; c < CK_BN / 32; ++c) tc::ld_32x32b_x32(tt + (uint32_t)(c * 32), sr + 32 * c);
-        tc::wait_ld();
-        if (lim < CK_BN - 1) {
+          for (int c = 0; c < CK_BN / 32; ++c) tc::ld_32x32b_x32(tt + (uint32_t)(c * 32), sr + 32 * c);
+          tc::wait_ld();
+          if (lim < CK_BN - 1) {
 #pragma unroll
-          for (int c = 0; c < CK_BN; ++c)
-            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < CK_BN; ++c)
+              if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < CK_BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          // running maximum in the exp2 domain, raised lazily
+          const float mnew = fmaxf(m, mx * sl2);
+          resc = mnew > m + CK_SLACK;
+          if (resc) {
+            alpha = fast_exp2(m - mnew);
+            m = mnew;
+          }
+          // P = exp2(s * scale * log2 e - m), 32 keys at a time: hi + lo pairs
+          // of the cache dtype, or (P16) f16 pairs with the row sum taken over
+          // the rounded values (each output row is then an exact convex
+          // combination)
+          const float2 negm = make_float2(-m, -m);
+#pragma unroll
+          for (int c = 0; c < CK_BN / 32; ++c) {
+            uint32_t hiw[16], low[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int k0 = 32 * c + 2 * e;
+              const float2 v = fma2(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+                                    sl2x2, negm);
+              const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+              if constexpr (P16) {
+                hiw[e] = Mma<__half>::pack(pe.x, pe.y);
+                const float2 hf = Widen<__half>::pair(hiw[e]);
+                lsum[e & 1] = make_float2(lsum[e & 1].x + hf.x, lsum[e & 1].y + hf.y);
+              } else {
+                lsum[e & 1] = make_float2(lsum[e & 1].x + pe.x, lsum[e & 1].y + pe.y);
+                hiw[e] = Mma<T>::pack(pe.x, pe.y);
+                const float2 hf = Widen<T>::pair(hiw[e]);
+                low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
+              }
+            }
+            tc::st_32x32b_x16(tt + (uint32_t)(16 * c), hiw);
+            if (!P16) tc::st_32x32b_x16(tt + C::COL_PL + (uint32_t)(16 * c), low);
+          }
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        l = l * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
+        // O_x is quiet: the P_x V before this S_x has completed
+        if (j > 0 && __any_sync(FULL_MASK, resc)) {
+          uint32_t o[32];
 #pragma unroll
-        for (int c = 0; c < CK_BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        // running maximum in the exp2 domain, raised lazily
-        const float mnew = fmaxf(m, mx * sl2);
-        resc = mnew > m + CK_SLACK;
-        if (resc) {
-          alpha = fast_exp2(m - mnew);
-          m = mnew;
+          for (int c = 0; c < D / 32; ++c) {
+            const uint32_t ta = tt + C::COL_O + (uint32_t)(c * 32);
+            tc::ld_32x32b_x32(ta, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::st_32x32b_x32(ta, o);
+          }
         }
-        // P = exp2(s * scale * log2 e - m), 32 keys at a time: hi + lo pairs
-        // of the cache dtype, or (P16) f16 pairs with the row sum taken over
-        // the rounded values (each output row is then an exact convex
-        // combination)
-        const float2 negm = make_float2(-m, -m);
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(CB_PF + x));
+      }
+      // ---- epilogue: O_x / l_x
+      if (x < ntile && ok) {
+        if (!warp_wait(bar(CB_OF + x), 0)) {
+          ok = false;
+        } else {
+          tc::fence_after_sync();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const size_t row = ((size_t)(q0 + (valid ? tok : 0)) * p.num_q_heads +
+                              (size_t)kvh * G + g) * (size_t)D;
+          uint32_t o[32];
+          float v[32];
 #pragma unroll
-        for (int c = 0; c < CK_BN / 32; ++c) {
-          uint32_t hiw[16], low[16];
+          for (int c = 0; c < D / 32; ++c) {
+            tc::ld_32x32b_x32(tt + C::COL_O + (uint32_t)(c * 32), o);
+            tc::wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int k0 = 32 * c + 2 * e;
-            const float2 v = fma2(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+            if (valid) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
+          }
+        }
+      }
+    } else {
+      // (f16 P with a converted bf16 V: the converting warps leave fewer
+      // registers, so the two warpgroups split each tile's key columns and
+      // take tile A, then tile B, agreeing on a row's maximum through shared
+      // memory.)
+      constexpr int HC = CK_BN / 2;             // key columns per thread
+      constexpr int HD = D / 2;                 // output columns per thread
+      const int wg = warp >> 2;
+      const int r = tid & (CK_ROWS - 1);        // query row = TMEM lane
+      const int tl = r / G, g = r % G;
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t pair = bar(CB_PAIR + (warp & 3));
+      float *red = reinterpret_cast<float *>(sm + C::OFF_RED);   // [2][2][128]
+      const float sl2 = p.scale_log2;
+      bool valid[2];
+      int tok[2], p_row[2];
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      for (int x = 0; x < 2; ++x) {
+        tok[x] = tb[x] + tl;
+        valid[x] = x < ntile && tl < TQ && tok[x] < te[x];
+        p_row[x] = valid[x] ? (L - n + tok[x]) : pm[x];
+      }
+      int round = 0;                            // row-statistics exchanges so far
+      // the two threads of a row combine v (max or sum) through shared memory
+      auto exchange = [&](float v, bool is_max) -> float {
+        float *rb = red + (round & 1) * 2 * CK_ROWS;
+        rb[wg * CK_ROWS + r] = v;
+        mbar_arrive(pair);
+        if (!warp_wait(pair, (uint32_t)round & 1u)) ok = false;
+        ++round;
+        const float o = rb[(wg ^ 1) * CK_ROWS + r];
+        return is_max ? fmaxf(v, o) : v + o;
+      };
+      uint32_t sr[HC];
+      for (int j = 0; j < nkv && ok; ++j) {
+        for (int x = 0; x < ntile && ok; ++x) {
+          if (j >= nk[x]) continue;
+          const uint32_t tt = tmem + lane_base + (uint32_t)x * C::TILE_COLS;
+          if (!warp_wait(bar(CB_SF + x), (uint32_t)j & 1u)) { ok = false; break; }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c) tc::ld_32x32b_x32(tt + (uint32_t)(wg * HC + c * 32), sr + 32 * c);
+          tc::wait_ld();
+          const int lim = p_row[x] - j * CK_BN - wg * HC;   // own columns 0..lim are visible
+          if (lim < HC - 1) {
+#pragma unroll
+            for (int c = 0; c < HC; ++c)
+              if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < HC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+          // both threads have read their S columns once they meet, so P may
+          // then overwrite any of the row's S columns
+          const float mx = exchange(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), true);
+          if (!ok) break;
+          // running maximum in the exp2 domain, raised lazily
+          const float mnew = fmaxf(m[x], mx * sl2);
+          const bool resc = mnew > m[x] + CK_SLACK;
+          float alpha = 1.f;
+          if (resc) {
+            alpha = fast_exp2(m[x] - mnew);
+            m[x] = mnew;
+          }
+          // P = exp2(s * scale * log2 e - m): as hi + lo pairs of the cache
+          // dtype, or (P16) as f16 pairs with the row sum taken over the
+          // rounded values (each output row is then an exact convex combination)
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m[x], -m[x]);
+          float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          uint32_t hiw[HC / 2], low[HC / 2];
+#pragma unroll
+          for (int e = 0; e < HC / 2; ++e) {
+            const float2 v = fma2(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                                   sl2x2, negm);
             const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
             if constexpr (P16) {
@@ -540,178 +675,48 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
               low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
             }
           }
-          tc::st_32x32b_x16(tt + (uint32_t)(16 * c), hiw);
-          if (!P16) tc::st_32x32b_x16(tt + C::COL_PL + (uint32_t)(16 * c), low);
+          l[x] = l[x] * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
+          // O_x is quiet: the P_x V before this S_x has completed
+          if (j > 0 && __any_sync(FULL_MASK, resc)) {
+            uint32_t o[32];
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+              const uint32_t ta = tt + C::COL_O + (uint32_t)(wg * HD + c * 32);
+              tc::ld_32x32b_x32(ta, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::st_32x32b_x32(ta, o);
+            }
+          }
+          tc::st_32x32b_x32(tt + (uint32_t)(wg * (HC / 2)), hiw);
+          if (!P16) tc::st_32x32b_x32(tt + C::COL_PL + (uint32_t)(wg * (HC / 2)), low);
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(CB_PF + x));
         }
       }
-      l = l * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
-      // O_x is quiet: the P_x V before this S_x has completed
-      if (j > 0 && __any_sync(FULL_MASK, resc)) {
-        uint32_t o[32];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint32_t ta = tt + C::COL_O + (uint32_t)(c * 32);
-          tc::ld_32x32b_x32(ta, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tc::st_32x32b_x32(ta, o);
-        }
-      }
-      tc::wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(CB_PF + x));
-    }
-    // ---- epilogue: O_x / l_x
-    if (x < ntile && ok) {
-      if (!warp_wait(bar(CB_OF + x), 0)) {
-        ok = false;
-      } else {
+      // ---- epilogue: O_x / l_x, a row's sum being its two threads' partial sums
+      for (int x = 0; x < ntile && ok; ++x) {
+        l[x] = exchange(l[x], false);
+        if (!ok || !warp_wait(bar(CB_OF + x), 0)) { ok = false; break; }
         tc::fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t row = ((size_t)(q0 + (valid ? tok : 0)) * p.num_q_heads +
-                            (size_t)kvh * G + g) * (size_t)D;
+        const uint32_t tt = tmem + lane_base + (uint32_t)x * C::TILE_COLS;
+        const float inv = l[x] > 0.f ? 1.f / l[x] : 0.f;
+        const size_t row = ((size_t)(q0 + (valid[x] ? tok[x] : 0)) * p.num_q_heads +
+                            (size_t)kvh * G + g) * (size_t)D + (size_t)(wg * HD);
         uint32_t o[32];
         float v[32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tc::ld_32x32b_x32(tt + C::COL_O + (uint32_t)(c * 32), o);
+        for (int c = 0; c < HD / 32; ++c) {
+          tc::ld_32x32b_x32(tt + C::COL_O + (uint32_t)(wg * HD + c * 32), o);
           tc::wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
-          if (valid) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
+          if (valid[x]) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
         }
       }
-    }
-    } else {
-    // (f16 P with a converted bf16 V: the converting warps leave fewer
-    // registers, so the two warpgroups split each tile's key columns and
-    // take tile A, then tile B, agreeing on a row's maximum through shared
-    // memory.)
-    constexpr int HC = CK_BN / 2;             // key columns per thread
-    constexpr int HD = D / 2;                 // output columns per thread
-    const int wg = warp >> 2;
-    const int r = tid & (CK_ROWS - 1);        // query row = TMEM lane
-    const int tl = r / G, g = r % G;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t pair = bar(CB_PAIR + (warp & 3));
-    float *red = reinterpret_cast<float *>(sm + C::OFF_RED);   // [2][2][128]
-    const float sl2 = p.scale_log2;
-    bool valid[2];
-    int tok[2], p_row[2];
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    for (int x = 0; x < 2; ++x) {
-      tok[x] = tb[x] + tl;
-      valid[x] = x < ntile && tl < TQ && tok[x] < te[x];
-      p_row[x] = valid[x] ? (L - n + tok[x]) : pm[x];
-    }
-    int round = 0;                            // row-statistics exchanges so far
-    // the two threads of a row combine v (max or sum) through shared memory
-    auto exchange = [&](float v, bool is_max) -> float {
-      float *rb = red + (round & 1) * 2 * CK_ROWS;
-      rb[wg * CK_ROWS + r] = v;
-      mbar_arrive(pair);
-      if (!warp_wait(pair, (uint32_t)round & 1u)) ok = false;
-      ++round;
-      const float o = rb[(wg ^ 1) * CK_ROWS + r];
-      return is_max ? fmaxf(v, o) : v + o;
-    };
-    uint32_t sr[HC];
-    for (int j = 0; j < nkv && ok; ++j) {
-      for (int x = 0; x < ntile && ok; ++x) {
-        if (j >= nk[x]) continue;
-        const uint32_t tt = tmem + lane_base + (uint32_t)x * C::TILE_COLS;
-        if (!warp_wait(bar(CB_SF + x), (uint32_t)j & 1u)) { ok = false; break; }
-        tc::fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < HC / 32; ++c) tc::ld_32x32b_x32(tt + (uint32_t)(wg * HC + c * 32), sr + 32 * c);
-        tc::wait_ld();
-        const int lim = p_row[x] - j * CK_BN - wg * HC;   // own columns 0..lim are visible
-        if (lim < HC - 1) {
-#pragma unroll
-          for (int c = 0; c < HC; ++c)
-            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < HC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
-        // both threads have read their S columns once they meet, so P may
-        // then overwrite any of the row's S columns
-        const float mx = exchange(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), true);
-        if (!ok) break;
-        // running maximum in the exp2 domain, raised lazily
-        const float mnew = fmaxf(m[x], mx * sl2);
-        const bool resc = mnew > m[x] + CK_SLACK;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = fast_exp2(m[x] - mnew);
-          m[x] = mnew;
-        }
-        // P = exp2(s * scale * log2 e - m): as hi + lo pairs of the cache
-        // dtype, or (P16) as f16 pairs with the row sum taken over the
-        // rounded values (each output row is then an exact convex combination)
-        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m[x], -m[x]);
-        float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        uint32_t hiw[HC / 2], low[HC / 2];
-#pragma unroll
-        for (int e = 0; e < HC / 2; ++e) {
-          const float2 v = fma2(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
-                                sl2x2, negm);
-          const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
-          if constexpr (P16) {
-            hiw[e] = Mma<__half>::pack(pe.x, pe.y);
-            const float2 hf = Widen<__half>::pair(hiw[e]);
-            lsum[e & 1] = make_float2(lsum[e & 1].x + hf.x, lsum[e & 1].y + hf.y);
-          } else {
-            lsum[e & 1] = make_float2(lsum[e & 1].x + pe.x, lsum[e & 1].y + pe.y);
-            hiw[e] = Mma<T>::pack(pe.x, pe.y);
-            const float2 hf = Widen<T>::pair(hiw[e]);
-            low[e] = Mma<T>::pack(pe.x - hf.x, pe.y - hf.y);
-          }
-        }
-        l[x] = l[x] * alpha + ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y));
-        // O_x is quiet: the P_x V before this S_x has completed
-        if (j > 0 && __any_sync(FULL_MASK, resc)) {
-          uint32_t o[32];
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            const uint32_t ta = tt + C::COL_O + (uint32_t)(wg * HD + c * 32);
-            tc::ld_32x32b_x32(ta, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::st_32x32b_x32(ta, o);
-          }
-        }
-        tc::st_32x32b_x32(tt + (uint32_t)(wg * (HC / 2)), hiw);
-        if (!P16) tc::st_32x32b_x32(tt + C::COL_PL + (uint32_t)(wg * (HC / 2)), low);
-        tc::wait_st();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(CB_PF + x));
-      }
-    }
-    // ---- epilogue: O_x / l_x, a row's sum being its two threads' partial sums
-    for (int x = 0; x < ntile && ok; ++x) {
-      l[x] = exchange(l[x], false);
-      if (!ok || !warp_wait(bar(CB_OF + x), 0)) { ok = false; break; }
-      tc::fence_after_sync();
-      const uint32_t tt = tmem + lane_base + (uint32_t)x * C::TILE_COLS;
-      const float inv = l[x] > 0.f ? 1.f / l[x] : 0.f;
-      const size_t row = ((size_t)(q0 + (valid[x] ? tok[x] : 0)) * p.num_q_heads +
-                          (size_t)kvh * G + g) * (size_t)D + (size_t)(wg * HD);
-      uint32_t o[32];
-      float v[32];
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        tc::ld_32x32b_x32(tt + C::COL_O + (uint32_t)(wg * HD + c * 32), o);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
-        if (valid[x]) store_row32(p.out, row + (size_t)c * 32, p.out_dtype, v);
-      }
-    }
     }
     if (!ok && lane == 0) atomicOr(p.flags, PKV_FLAG_TIMEOUT);
   }
