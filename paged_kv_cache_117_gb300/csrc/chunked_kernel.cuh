@@ -45,8 +45,8 @@
 // issuing and drains what it has in flight before the CTA frees its TMEM and
 // exits.
 //
-// Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, K 3 x 32 KiB, V
-// 2 x 32 KiB, in the 128-byte swizzled layout (rows of 64 elements); one CTA
+// Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, K 2 x 32 KiB, V
+// 3 x 32 KiB (V waits longer: a V stage is freed last, after P_B V), in the 128-byte swizzled layout (rows of 64 elements); one CTA
 // per SM.  TMEM columns: tile x at 256 x: S_x / P_x (P hi 0..63, P lo
 // 64..127), O_x at 128.
 #pragma once
@@ -68,8 +68,8 @@ constexpr int CK_CONV = 10;      // first V-converting warp (f16 P from a bf16 c
 // warps -- four (one per SM sub-partition) when a bf16 V tile is converted to
 // f16, two otherwise (then idle).
 __host__ __device__ constexpr int ck_threads(bool convert) { return convert ? 448 : 384; }
-constexpr int CK_KST = 3;        // K ring stages
-constexpr int CK_VST = 2;        // V ring stages
+constexpr int CK_KST = 2;        // K ring stages
+constexpr int CK_VST = 3;        // V ring stages
 constexpr float CK_SLACK = 8.0f; // lazy rescale threshold (log2 domain)
 
 template <int D>
