@@ -46,9 +46,9 @@
 // exits.
 //
 // Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, K 2 x 32 KiB, V
-// 3 x 32 KiB (V waits longer: a V stage is freed last, after P_B V), in the 128-byte swizzled layout (rows of 64 elements); one CTA
-// per SM.  TMEM columns: tile x at 256 x: S_x / P_x (P hi 0..63, P lo
-// 64..127), O_x at 128.
+// 3 x 32 KiB (a V stage is freed last, after P_B V), in the 128-byte
+// swizzled layout (rows of 64 elements); one CTA per SM.  TMEM columns: tile
+// x at 256 x: S_x / P_x (P hi 0..63, P lo 64..127), O_x at 128.
 #pragma once
 
 #include <type_traits>
