@@ -45,9 +45,10 @@
 // issuing and drains what it has in flight before the CTA frees its TMEM and
 // exits.
 //
-// Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, K 2 x 32 KiB, V
-// 3 x 32 KiB (a V stage is freed last, after P_B V), in the 128-byte
-// swizzled layout (rows of 64 elements); one CTA per SM.  TMEM columns: tile
+// Shared memory (head_dim 128): Q_A and Q_B 32 KiB each, five K/V stages of
+// 32 KiB (3 K + 2 V; 2 K + 3 V when V is converted, which then also waits
+// for its conversion), in the 128-byte swizzled layout (rows of 64
+// elements); one CTA per SM.  TMEM columns: tile
 // x at 256 x: S_x / P_x (P hi 0..63, P lo 64..127), O_x at 128.
 #pragma once
 
@@ -68,8 +69,12 @@ constexpr int CK_CONV = 10;      // first V-converting warp (f16 P from a bf16 c
 // warps -- four (one per SM sub-partition) when a bf16 V tile is converted to
 // f16, two otherwise (then idle).
 __host__ __device__ constexpr int ck_threads(bool convert) { return convert ? 448 : 384; }
-constexpr int CK_KST = 2;        // K ring stages
-constexpr int CK_VST = 3;        // V ring stages
+// K and V rings share five tile stages: 3 K + 2 V, or 2 K + 3 V when V is
+// converted to f16 (a V stage then also waits for its conversion)
+constexpr int CK_STAGES = 5;
+constexpr int CK_ST_MAX = 3;     // barrier slots per ring
+__host__ __device__ constexpr int ck_kst(bool convert) { return convert ? 2 : 3; }
+__host__ __device__ constexpr int ck_vst(bool convert) { return CK_STAGES - ck_kst(convert); }
 constexpr float CK_SLACK = 8.0f; // lazy rescale threshold (log2 domain)
 
 template <int D>
@@ -80,9 +85,8 @@ struct ChunkCfg {
   static constexpr int KV_BYTES = NH * HALF;
   static constexpr int OFF_Q = 0;              // Q_A, then Q_B
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + CK_KST * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + CK_VST * KV_BYTES;
-  static constexpr int NBAR = 24;
+  static constexpr int OFF_BAR = OFF_K + CK_STAGES * KV_BYTES;   // K stages, then V stages
+  static constexpr int NBAR = 26;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   // (V converted) row-maximum exchange of the two softmax warpgroups:
   // [2 rounds][2][128]
@@ -97,16 +101,16 @@ struct ChunkCfg {
 // mbarrier slots
 enum : int {
   CB_Q = 0,                  // both Q tiles landed (tx)
-  CB_KF = 1,                 // K stage full [CK_KST] (tx)
-  CB_KE = CB_KF + CK_KST,    // K stage free [CK_KST] (MMA commit)
-  CB_VF = CB_KE + CK_KST,    // V stage full [CK_VST] (tx)
-  CB_VE = CB_VF + CK_VST,    // V stage free [CK_VST] (MMA commit)
-  CB_SF = CB_VE + CK_VST,    // S_x computed [2: tiles A, B] (MMA commit)
+  CB_KF = 1,                 // K stage full [K stages] (tx)
+  CB_KE = CB_KF + CK_ST_MAX, // K stage free [K stages] (MMA commit)
+  CB_VF = CB_KE + CK_ST_MAX, // V stage full [V stages] (tx)
+  CB_VE = CB_VF + CK_ST_MAX, // V stage free [V stages] (MMA commit)
+  CB_SF = CB_VE + CK_ST_MAX, // S_x computed [2: tiles A, B] (MMA commit)
   CB_PF = CB_SF + 2,         // P_x written [2] (one arrival per softmax warp writing P_x)
   CB_OF = CB_PF + 2,         // O_x final [2] (MMA commit)
   CB_PAIR = CB_OF + 2,       // (V converted) row-maximum exchange of warps w, w + 4 [4] (64 arrivals)
-  CB_VC = CB_PAIR + 4,       // V stage converted to f16 [CK_VST] (one arrival per converting thread)
-  CB_COUNT = CB_VC + CK_VST,
+  CB_VC = CB_PAIR + 4,       // V stage converted to f16 [V stages] (one arrival per converting thread)
+  CB_COUNT = CB_VC + CK_ST_MAX,
 };
 
 // Every lane of the warp waits; the result is the same on all lanes.
@@ -152,6 +156,8 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   constexpr bool CONVERT = P16 && BF16;
   constexpr int NT = ck_threads(CONVERT);
   constexpr int NCONV = NT - CK_CONV * 32;       // converting threads
+  constexpr int CK_KST = ck_kst(CONVERT), CK_VST = ck_vst(CONVERT);
+  constexpr int OFF_V = C::OFF_K + CK_KST * C::KV_BYTES;
   static_assert(B * 128 % 1024 == 0, "boxes land on 1 KiB boundaries (128-byte swizzle atoms)");
   constexpr int BLOCKS_PER_TILE = CK_BN / B;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       }
       if (lane == 0) mbar_arrive_expect_tx(bar(CB_VF + vs), (uint32_t)C::KV_BYTES);
       __syncwarp();
-      load_tile(&vmap, sb + C::OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
+      load_tile(&vmap, sb + OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
       nv_issued = j + 1;
     }
     // drain: every load issued has landed before the CTA may exit (loads
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       return (uint32_t)tc::sdesc_sw128(sb + C::OFF_K + (j % CK_KST) * C::KV_BYTES, 16, 1024);
     };
     auto v_lo = [&](int j) {
-      return (uint32_t)tc::sdesc_sw128(sb + C::OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
+      return (uint32_t)tc::sdesc_sw128(sb + OFF_V + (j % CK_VST) * C::KV_BYTES, C::HALF, 1024);
     };
     auto issue_s = [&](int x, uint32_t lk) {     // S_x = Q_x K^T, K's stage low word lk
       if (lane == 0) {
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
         // V rows past the sequence hold whatever the pool holds there; their
         // probabilities are exactly zero, but 0 * NaN is not, so zero them
         const int z0 = L - j * CK_BN;
-        unsigned char *vsm = sm + C::OFF_V + (j % CK_VST) * C::KV_BYTES;
+        unsigned char *vsm = sm + OFF_V + (j % CK_VST) * C::KV_BYTES;
         for (int x = lane; x < (CK_BN - z0) * 8 * C::NH; x += 32) {
           const int h = x / ((CK_BN - z0) * 8), rem = x % ((CK_BN - z0) * 8);
           *reinterpret_cast<uint4 *>(vsm + h * C::HALF + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       for (int j = 0; j < nkv && ok; ++j) {
         const int vs = j % CK_VST;
         if (!warp_wait(bar(CB_VF + vs), (uint32_t)(j / CK_VST) & 1u)) { ok = false; break; }
-        unsigned char *vsm = sm + C::OFF_V + vs * C::KV_BYTES;
+        unsigned char *vsm = sm + OFF_V + vs * C::KV_BYTES;
         const int live = min(CK_BN, L - j * CK_BN);  // rows holding tokens of the sequence
 #pragma unroll 4
         for (int c = ct; c < CK_BN * 8 * C::NH; c += NCONV) {
