@@ -249,11 +249,16 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   const uint32_t tmem = *tslot;
   bool ok = true;
 
-  if (warp == CK_PRODUCER) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop: lane i holds block-table entry i of the
-    // current group of 32 (TPG tiles), the next group's entries are already
-    // in flight, and the lanes issue the TMA loads.
+  if (warp == CK_PRODUCER || (!CONVERT && warp == CK_CONV)) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 loads the Q tiles and the K tiles, warp 10 the V tiles (when it
+    // does not convert V; then warp 8 loads both), so that K runs ahead of V
+    // as far as its ring allows.  A producer warp runs the loop as a whole:
+    // lane i holds block-table entry i of the current group of 32 (TPG
+    // tiles), the next group's entries are already in flight, and the lanes
+    // issue the TMA loads.
+    const bool do_k = warp == CK_PRODUCER;
+    const bool do_v = warp == CK_CONV || CONVERT;
     constexpr int TPG = 32 / BLOCKS_PER_TILE;    // tiles per group of 32 entries
     const int32_t *tbl = p.block_tables + (size_t)s * p.max_blocks;
     const int nb_used = min(nb_valid, nkv * BLOCKS_PER_TILE);
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       }
       return blk;
     };
-    if (lane == 0) {
+    if (do_k && lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
@@ -303,27 +308,31 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       for (int b = 0; b < BLOCKS_PER_TILE; ++b)
         blk[b] = __shfl_sync(FULL_MASK, cur, (j % TPG) * BLOCKS_PER_TILE + b);
       const int ks = j % CK_KST, vs = j % CK_VST;
-      if (j >= CK_KST && !warp_wait(bar(CB_KE + ks), ((uint32_t)(j / CK_KST) & 1u) ^ 1u)) {
-        ok = false;
-        break;
+      if (do_k) {
+        if (j >= CK_KST && !warp_wait(bar(CB_KE + ks), ((uint32_t)(j / CK_KST) & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(CB_KF + ks), (uint32_t)C::KV_BYTES);
+        __syncwarp();
+        load_tile(&kmap, sb + C::OFF_K + ks * C::KV_BYTES, blk, bar(CB_KF + ks));
+        nk_issued = j + 1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(CB_KF + ks), (uint32_t)C::KV_BYTES);
-      __syncwarp();
-      load_tile(&kmap, sb + C::OFF_K + ks * C::KV_BYTES, blk, bar(CB_KF + ks));
-      nk_issued = j + 1;
-      if (j >= CK_VST && !warp_wait(bar(CB_VE + vs), ((uint32_t)(j / CK_VST) & 1u) ^ 1u)) {
-        ok = false;
-        break;
+      if (do_v) {
+        if (j >= CK_VST && !warp_wait(bar(CB_VE + vs), ((uint32_t)(j / CK_VST) & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(CB_VF + vs), (uint32_t)C::KV_BYTES);
+        __syncwarp();
+        load_tile(&vmap, sb + OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
+        nv_issued = j + 1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(CB_VF + vs), (uint32_t)C::KV_BYTES);
-      __syncwarp();
-      load_tile(&vmap, sb + OFF_V + vs * C::KV_BYTES, blk, bar(CB_VF + vs));
-      nv_issued = j + 1;
     }
     // drain: every load issued has landed before the CTA may exit (loads
     // older than a ring's worth were consumed, so they have landed)
     if (lane == 0) {
-      mbar_wait_bounded(bar(CB_Q), 0);
+      if (do_k) mbar_wait_bounded(bar(CB_Q), 0);
       for (int j = max(0, nk_issued - CK_KST); j < nk_issued; ++j)
         mbar_wait_bounded(bar(CB_KF + j % CK_KST), (uint32_t)(j / CK_KST) & 1u);
       for (int j = max(0, nv_issued - CK_VST); j < nv_issued; ++j)
