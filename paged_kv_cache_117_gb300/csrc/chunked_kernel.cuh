@@ -35,9 +35,10 @@
 // side by side.  (When V is converted, the four extra warps leave fewer
 // registers: there thread t of warpgroup wg owns key columns wg*64 ..
 // wg*64+63 of row t % 128 of both tiles, and the two threads of a row agree
-// on its maximum through shared memory.)  Warp 8 issues the TMA loads (the
-// two Q tiles once; K and V tiles through rings, one box per block (all its
-// tokens) and 64 dims, the block-table entries fetched a group of 32 ahead).
+// on its maximum through shared memory.)  Warp 8 issues the TMA loads of the
+// two Q tiles (once) and of the K tiles, warp 10 those of the V tiles (warp
+// 8 both when warp 10 converts V), through rings, one box per block (all its
+// tokens) and 64 dims, the block-table entries fetched a group of 32 ahead.
 // Warp 9 allocates TMEM and issues the MMAs (one lane).  Warps 10-13 convert
 // V tiles to f16 when P goes in as f16 and the cache is bf16 (otherwise
 // warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is
