@@ -40,8 +40,8 @@
 // 8 both when warp 10 converts V), through rings, one box per block (all its
 // tokens) and 64 dims, the block-table entries fetched a group of 32 ahead.
 // Warp 9 allocates TMEM and issues the MMAs (one lane).  Warps 10-13 convert
-// V tiles to f16 when P goes in as f16 and the cache is bf16 (otherwise
-// warps 10-11 exist and idle).  All hand-offs are mbarriers; every wait is
+// V tiles to f16 when P goes in as f16 and the cache is bf16; otherwise warp
+// 10 loads V and warp 11 idles.  All hand-offs are mbarriers; every wait is
 // bounded and a timeout sets PKV_FLAG_TIMEOUT, after which each role stops
 // issuing and drains what it has in flight before the CTA frees its TMEM and
 // exits.
