@@ -114,6 +114,14 @@ enum : int {
   CB_COUNT = CB_VC + CK_ST_MAX,
 };
 
+// max(a, b, c) in one instruction (sm_100 and later); like fmaxf, a NaN
+// operand is ignored
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Every lane of the warp waits; the result is the same on all lanes.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   const bool ok = mbar_wait_bounded(bar, parity);
@@ -394,8 +402,21 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     auto wait_k = [&](int j) {
       return warp_wait(bar(CB_KF + j % CK_KST), (uint32_t)(j / CK_KST) & 1u);
     };
+    // Up to three barriers polled together with one vote at the end: in this
+    // warp, which shares its issue slots with two softmax warps, even a
+    // satisfied wait-and-vote costs ~150-230 cycles (measured).
+    auto wait3 = [&](uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, bool use2, uint32_t b2,
+                     uint32_t p2) {
+      bool d0 = false, d1 = false, d2 = !use2;
+      for (uint32_t it = 0; it < WAIT_LIMIT && !(d0 && d1 && d2); ++it) {
+        if (!d0) d0 = mbar_try_wait(b0, p0);
+        if (!d1) d1 = mbar_try_wait(b1, p1);
+        if (!d2) d2 = mbar_try_wait(b2, p2);
+      }
+      return __all_sync(FULL_MASK, d0 && d1 && d2);
+    };
     const int tail_tile = (L % CK_BN) ? (L - 1) / CK_BN : -1;
-    ok = warp_wait(bar(CB_Q), 0) && wait_k(0);
+    ok = wait3(bar(CB_Q), 0, bar(CB_KF + 0), 0, false, 0, 0);
     if (ok) {
       tc::fence_after_sync();
       issue_s(0, k_lo(0));
@@ -408,8 +429,9 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       // V(j), P_A(j) and K(j + 1) (usually long landed) are all waited for
       // first, so that P_A(j) V(j) and S_A(j + 1) issue back to back
       const bool next_a = j + 1 < nk[0];
-      if (!warp_wait(bar((CONVERT ? CB_VC : CB_VF) + j % CK_VST), (uint32_t)(j / CK_VST) & 1u) ||
-          !warp_wait(bar(CB_PF + 0), (uint32_t)j & 1u) || (next_a && !wait_k(j + 1))) {
+      if (!wait3(bar((CONVERT ? CB_VC : CB_VF) + j % CK_VST), (uint32_t)(j / CK_VST) & 1u,
+                 bar(CB_PF + 0), (uint32_t)j & 1u, next_a, bar(CB_KF + (j + 1) % CK_KST),
+                 (uint32_t)((j + 1) / CK_KST) & 1u)) {
         ok = false;
         break;
       }
@@ -527,7 +549,8 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
           }
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < CK_BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+          for (int c = 0; c < CK_BN; c += 2)
+            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
           const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           // running maximum in the exp2 domain, raised lazily
           const float mnew = fmaxf(m, mx * sl2);
@@ -656,7 +679,8 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
           }
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < HC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+          for (int c = 0; c < HC; c += 2)
+            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
           // both threads have read their S columns once they meet, so P may
           // then overwrite any of the row's S columns
           const float mx = exchange(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), true);
