@@ -103,6 +103,13 @@ def test_wide_table_and_long_context():
     _run(_w(8, 2, 128, 16, N=800), [2900, 0], [100, 50], width=300)
 
 
+@pytest.mark.parametrize("p_format", ["hilo", "f16"])
+def test_longest_context(p_format):
+    # 300 queries after 30,000 cached tokens (237 KV tiles, a 1,894-block table
+    # row) next to two single-token decodes
+    _run(_w(8, 2, 128, 16, N=2400), [30000, 0, 7], [300, 1, 1], p_format=p_format)
+
+
 def test_prefill_full_size_sampled():
     """The benchmark's prefill workload at full size, in its launch
     configuration (16 chunks of 512 tokens after up to 7,168 cached tokens,

@@ -188,6 +188,40 @@ def test_workload_full_size_sampled(name):
         gh.assert_close_to_oracle(out16[seqs], ref.out, ATOL)
 
 
+@pytest.mark.parametrize("pt,append", [(512, False), (0, False), (512, True)])
+def test_longest_contexts_with_needles(pt, append):
+    """Contexts far beyond the workloads': 131,072 tokens (256 partitions of
+    512, or a single unit streaming all of it), 65,537 (its new token opens a
+    fresh block), one token only, and 4,097.  In KV head 0 one key of each
+    long sequence is planted to score ~90 above the rest, deep inside the
+    context, so that one far partition dominates the merge."""
+    lens = (131072, 65537, 1, 4097)
+    nb = sum((L + 15) // 16 for L in lens)
+    w = wl.Workload("longest", 4, 32, 8, 128, 16, nb + 64, torch.bfloat16, pt, 126,
+                    "fixed", lens)
+    plan = gh.plan_step(w)
+    k, v = wl.make_pool_chunked(w, "cuda")
+    q, key, value = wl.make_step_inputs(w, "cuda")
+    for s, pos in ((0, 100_000), (1, 3), (3, 4000)):
+        blk = plan.tables[s][pos // w.block_size]
+        k[blk, pos % w.block_size, 0] = (q[s, 0].float() * 8).to(w.dtype)
+    seqs = list(range(w.num_seqs))
+    ids = gh.needed_blocks(plan, seqs)
+    idx = torch.tensor(ids, device="cuda")
+    kb, vb = k[idx].cpu(), v[idx].cpu()            # inputs, before any library kernel
+    ref = gh.oracle_step(plan, kb, vb, ids, q.cpu(), key.cpu(), value.cpu(), seqs)
+    # the needles dominate: query head 0 of sequence 0 returns (nearly) its V row
+    pos = 100_000
+    vrow = vb[ids.index(plan.tables[0][pos // 16]), pos % 16, 0].double()
+    assert (ref.out[0, 0] - vrow).abs().max().item() < 1e-3
+    out = gh.run_gpu_step(plan, k, v, q, key, value, torch.float32, append=append)
+    torch.cuda.synchronize()
+    assert _flags() == 0
+    gh.assert_close_to_oracle(out, ref.out, ATOL)
+    assert torch.equal(k[idx].cpu(), ref.k_blocks)
+    assert torch.equal(v[idx].cpu(), ref.v_blocks)
+
+
 # ---- write and copy on their own: whole pool, bit-exact ---------------------
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
