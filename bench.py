@@ -22,6 +22,7 @@ on a bounded sample of the same workload instead.
                     [--workload llama8b]
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -96,7 +97,47 @@ def parse_args():
                     help="chunked workloads: P as hi + lo 16-bit operands, or as one f16 operand")
     ap.add_argument("--graph", action="store_true",
                     help="capture the whole step (all layers) in one CUDA graph and replay it")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="decode workloads of independent sequences: this many sequences "
+                         "(the workload's length distribution unless --context is given)")
+    ap.add_argument("--context", type=int, default=None,
+                    help="decode workloads of independent sequences: every sequence this "
+                         "long (tokens, counting this step's)")
     return ap.parse_args()
+
+
+def select_workload(a):
+    """The named workload, or (--seqs / --context) a copy of a decode
+    workload of independent sequences with another batch or length: the same
+    heads, dims, dtype, block size and partition, a pool large enough for
+    every sequence, and a name that says so (no committed profile applies)."""
+    w = wl.WORKLOADS[a.workload]
+    if a.seqs is None and a.context is None:
+        return w
+    if w.lens_kind not in ("fixed", "uniform", "lognormal"):
+        raise SystemExit("--seqs / --context apply to the decode workloads of independent "
+                         "sequences (tiny, opt13b, llama8b, qwen72b)")
+    S = a.seqs if a.seqs is not None else w.num_seqs
+    if S <= 0 or (a.context is not None and a.context <= 0):
+        raise SystemExit("--seqs and --context must be positive")
+    if a.context is not None:
+        lk, args, name = "fixed", (a.context,) * S, f"{w.name}-{S}x{a.context}"
+    else:
+        lk, args, name = w.lens_kind, w.lens_args, f"{w.name}-{S}seqs"
+    hi = max(args) if lk == "fixed" else (args[1] if lk == "uniform" else args[3])
+    blocks = S * -(-hi // w.block_size)
+    return dataclasses.replace(w, name=name, num_seqs=S, lens_kind=lk, lens_args=args,
+                               num_blocks=max(w.num_blocks if lk != "fixed" else 0,
+                                              blocks + blocks // 8 + 64))
+
+
+def width_tokens(w):
+    """Block-table row width in tokens: the workload's, or the longest
+    possible sequence of a resized one."""
+    if w.name in TABLE_WIDTH_TOKENS:
+        return TABLE_WIDTH_TOKENS[w.name]
+    return max(w.lens_args) if w.lens_kind == "fixed" else (
+        w.lens_args[1] if w.lens_kind == "uniform" else w.lens_args[3])
 
 
 # ---------------------------------------------------------------------------
@@ -105,7 +146,7 @@ def parse_args():
 def build_metadata(w):
     lens = wl.context_lens(w)
     tables = wl.scatter_block_tables(lens, w.block_size, wl.free_block_order(w))
-    width = -(-TABLE_WIDTH_TOKENS[w.name] // w.block_size)
+    width = -(-width_tokens(w) // w.block_size)
     return lens, tables, width
 
 
@@ -487,7 +528,7 @@ def run_native(a, world, rank, local):
     assert torch.cuda.is_available(), "the native benchmark needs a GPU"
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = wl.WORKLOADS[a.workload]
+    w = select_workload(a)
     pt = w.partition_tokens if a.partition is None else a.partition
     k, v = wl.make_pool_chunked(w, dev)
     hist = None
@@ -896,7 +937,7 @@ def run_reference(a, world, rank, local):
     """The fp64 CPU oracle as it stands, one bounded sample per step."""
     if rank != 0:
         return None
-    w = wl.WORKLOADS[a.workload]
+    w = select_workload(a)
     if w.lens_kind == "shared":
         lens, tables, width, slot_t, _, _ = build_shared_step(w)
     elif w.lens_kind == "beam":
@@ -980,6 +1021,9 @@ def main():
     a = parse_args()
     world, rank, local = dist_init()
     chunked = wl.WORKLOADS[a.workload].lens_kind in ("chunked", "prefix")
+    if chunked and (a.seqs is not None or a.context is not None):
+        raise SystemExit("--seqs / --context apply to the decode workloads of independent "
+                         "sequences (tiny, opt13b, llama8b, qwen72b)")
     if a.impl == "reference":
         res = (run_reference_chunked if chunked else run_reference)(a, world, rank, local)
     else:

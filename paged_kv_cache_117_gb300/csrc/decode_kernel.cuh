@@ -12,11 +12,11 @@
 // part_blocks blocks.  A work unit is (sequence, partition, KV head, chunk of
 // up to 16 query heads).  decode_plan_kernel (one CTA) lists the (sequence,
 // partition) items in the workspace -- all full partitions first, then the
-// shorter last partitions -- and resets the work counter and the per-sequence
-// completion counters.  decode_kernel runs as a persistent grid sized to fill
-// the SMs; each CTA takes units with atomicAdd, two ahead of the one it is
-// processing, so that every warp knows its next unit while it works on the
-// current one.
+// shorter last partitions, longest first -- and resets the work counter and
+// the per-sequence completion counters.  decode_kernel runs as a persistent
+// grid sized to fill the SMs; CTA c starts with units c and c + grid, then
+// takes units with atomicAdd, two ahead of the one it is processing, so that
+// every warp knows its next unit while it works on the current one.
 //
 // Streaming.  Warp w of the CTA takes blocks jb + w, jb + w + 4, ... of the
 // unit's partition, in chunks of up to 16 tokens, through a private ring of
@@ -122,9 +122,24 @@ struct DecodeCfg {
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
 // ---------------------------------------------------------------------------
-// Work list: one CTA of 1024 threads.
-static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
-  __shared__ int wsum_f[32], wsum_p[32];
+// Work list: one CTA of 1024 threads.  All full partitions come first (in
+// sequence order), then the shorter last partitions, longest first (a
+// counting sort over at most PLAN_BUCKETS length classes), so that the units
+// handed out last are the shortest and the CTAs run out of work at nearly the
+// same time.  The order changes no result: every unit is computed the same
+// way wherever it runs, and a sequence's records are merged in partition
+// order.
+constexpr int PLAN_BUCKETS = 1024;
+
+// Length class of a last partition of r blocks (0 < r < pb), of nbk <= pb
+// classes: the longer, the lower.
+__device__ __forceinline__ int plan_bucket(int r, int pb, int nbk) {
+  return (int)((long long)(pb - r) * nbk / pb);
+}
+
+static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const DecodeParams p) {
+  __shared__ int wsum[32];
+  __shared__ int slot[PLAN_BUCKETS];   // last partitions per length class, then the next free slot
   pdl_launch_dependents();   // the attention grid may start its prologue
   pdl_wait_predecessors();   // context_lens / out may come from earlier kernels
   const int S = p.num_seqs, PB = p.part_blocks, Bs = p.block_size;
@@ -132,15 +147,21 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int per = (S + 1023) / 1024;
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
-  int nf = 0, np = 0;
+  const int nbk = min(PB, PLAN_BUCKETS);
+  slot[tid] = 0;
+  __syncthreads();
+  int nf = 0;
   for (int s = s0; s < s1; ++s) {
     const int L0 = __ldg(p.context_lens + s);
     if (L0 < 0 || L0 > cap) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
     const int nb = (clamp_len(L0, cap) + Bs - 1) / Bs;
     nf += nb / PB;
-    np += (nb % PB) != 0;
+    if (nb % PB) atomicAdd(&slot[plan_bucket(nb % PB, PB, nbk)], 1);
   }
-  // block-wide exclusive scans of nf and np
+  __syncthreads();
+  // block-wide exclusive scans: full partitions per thread, last partitions
+  // per length class (thread t holds class t)
+  const int np = slot[tid];
   int xf = nf, xp = np;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -148,29 +169,31 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
     const int yp = __shfl_up_sync(FULL_MASK, xp, off);
     if (lane >= off) { xf += yf; xp += yp; }
   }
-  if (lane == 31) { wsum_f[wid] = xf; wsum_p[wid] = xp; }
+  __shared__ int wsum_p[32];
+  if (lane == 31) { wsum[wid] = xf; wsum_p[wid] = xp; }
   __syncthreads();
   if (wid == 0) {
-    int tf = wsum_f[lane], tp = wsum_p[lane];
+    int tf = wsum[lane], tp = wsum_p[lane];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int yf = __shfl_up_sync(FULL_MASK, tf, off);
       const int yp = __shfl_up_sync(FULL_MASK, tp, off);
       if (lane >= off) { tf += yf; tp += yp; }
     }
-    wsum_f[lane] = tf;   // inclusive over warps
+    wsum[lane] = tf;   // inclusive over warps
     wsum_p[lane] = tp;
   }
   __syncthreads();
-  const int total_f = wsum_f[31], total_p = wsum_p[31];
-  int fo = xf - nf + (wid ? wsum_f[wid - 1] : 0);
-  int po = total_f + xp - np + (wid ? wsum_p[wid - 1] : 0);
+  const int total_f = wsum[31], total_p = wsum_p[31];
+  int fo = xf - nf + (wid ? wsum[wid - 1] : 0);
+  slot[tid] = total_f + xp - np + (wid ? wsum_p[wid - 1] : 0);
+  __syncthreads();
   for (int s = s0; s < s1; ++s) {
     const int L = clamp_len(__ldg(p.context_lens + s), cap);
     const int nb = (L + Bs - 1) / Bs;
     const int F = nb / PB;
     for (int q = 0; q < F; ++q) p.items[fo++] = make_int2(s, q);
-    if (nb % PB) p.items[po++] = make_int2(s, F);
+    if (nb % PB) p.items[atomicAdd(&slot[plan_bucket(nb % PB, PB, nbk)], 1)] = make_int2(s, F);
     if (L == 0) {   // nothing to attend to: zeros
       const size_t base = (size_t)s * p.num_q_heads * p.head_dim;
       for (int e = 0; e < p.num_q_heads * p.head_dim; ++e)
@@ -179,7 +202,9 @@ static __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodePa
   }
   for (int i = tid; i < S * p.num_hc; i += 1024) p.seq_done[i] = 0u;
   if (tid == 0) {
-    p.ctrl[0] = 0u;
+    // CTA c of the attention grid starts with units c and c + grid without
+    // asking; the counter hands out the rest
+    p.ctrl[0] = 2u * (unsigned)p.grid;
     p.ctrl[1] = (unsigned)(total_f + total_p) * (unsigned)p.num_hc;
   }
 }
@@ -298,9 +323,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   // everything above is local; the work list, the pool and q come from the
   // kernels before this one
   pdl_wait_predecessors();
-  if (tid == 0) {
-    s_int[0] = (int)atomicAdd(p.ctrl, 1u);
-    s_int[1] = (int)atomicAdd(p.ctrl, 1u);
+  if (tid == 0) {   // the first two units need no atomic (the counter starts past them)
+    s_int[0] = (int)blockIdx.x;
+    s_int[1] = (int)(blockIdx.x + gridDim.x);
   }
   const unsigned total = __ldcg(p.ctrl + 1);
   __syncthreads();
@@ -742,16 +767,18 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
   LaunchInfo li;
   e = launch_info(reinterpret_cast<const void *>(kern), C::NW * 32, C::SMEM_BYTES, dev, &li);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, p);
-  if (e != cudaSuccess) return e;
-  ++*launches;
   const long long units_max =
       (long long)p.num_seqs * p.max_parts * p.num_hc;   // upper bound on work units
   long long grid = (long long)li.sms * li.ctas_per_sm;
   if (grid > units_max) grid = units_max;
   if (grid < 1) grid = 1;
+  DecodeParams pg = p;
+  pg.grid = (int)grid;
+  e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, pg);
+  if (e != cudaSuccess) return e;
+  ++*launches;
   e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::NW * 32), C::SMEM_BYTES, stream, kmap, vmap,
-                 p);
+                 pg);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaSuccess;

@@ -63,6 +63,7 @@ struct DecodeParams {
   float *part_ml;                // [S, Hq, max_parts, 2]  (running max, sum)
   float *part_o;                 // [S, Hq, max_parts, D]  unnormalised output
   unsigned *ctrl;                // [0] next work unit, [1] number of work units
+  int grid = 0;                  // CTAs of the attention grid (set at launch)
   unsigned *seq_done;            // [S, num_hc] partitions finished per sequence
   int2 *items;                   // [S * max_parts] (sequence, partition) work list
   unsigned *flags;               // device flag word
