@@ -11,9 +11,10 @@
 // Work decomposition.  A sequence's context is cut into partitions of
 // part_blocks blocks.  A work unit is (sequence, partition, KV head, chunk of
 // up to 16 query heads).  decode_plan_kernel (one CTA) lists the (sequence,
-// partition) items in the workspace -- all full partitions first, then the
-// shorter last partitions, longest first -- and resets the work counter and
-// the per-sequence completion counters.  decode_kernel runs as a persistent
+// partition) items in the workspace -- the full partitions of the sequences
+// that span several, then their shorter last partitions, then the
+// one-partition sequences, the last two groups longest first -- and resets
+// the work counter and the per-sequence completion counters.  decode_kernel runs as a persistent
 // grid sized to fill the SMs; CTA c starts with units c and c + grid, then
 // takes units with atomicAdd, two ahead of the one it is processing, so that
 // every warp knows its next unit while it works on the current one.
@@ -122,17 +123,19 @@ struct DecodeCfg {
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
 // ---------------------------------------------------------------------------
-// Work list: one CTA of 1024 threads.  All full partitions come first (in
-// sequence order), then the shorter last partitions, longest first (a
-// counting sort over at most PLAN_BUCKETS length classes), so that the units
-// handed out last are the shortest and the CTAs run out of work at nearly the
-// same time.  The order changes no result: every unit is computed the same
-// way wherever it runs, and a sequence's records are merged in partition
-// order.
+// Work list: one CTA of 1024 threads.  First the full partitions of the
+// sequences that span several partitions (in sequence order), then their
+// shorter last partitions, then the sequences that fit in one partition; the
+// last two groups longest first (a counting sort over PLAN_BUCKETS / 2
+// length classes each).  So the units handed out last are the shortest, and
+// they merge no partitions (a one-partition sequence writes its output
+// directly): the CTAs run out of work at nearly the same time.  The order
+// changes no result: every unit is computed the same way wherever it runs,
+// and a sequence's records are merged in partition order.
 constexpr int PLAN_BUCKETS = 1024;
 
-// Length class of a last partition of r blocks (0 < r < pb), of nbk <= pb
-// classes: the longer, the lower.
+// Length class of r blocks (0 < r < pb) among nbk <= pb classes: the longer,
+// the lower.
 __device__ __forceinline__ int plan_bucket(int r, int pb, int nbk) {
   return (int)((long long)(pb - r) * nbk / pb);
 }
@@ -147,7 +150,13 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int per = (S + 1023) / 1024;
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
-  const int nbk = min(PB, PLAN_BUCKETS);
+  const int nbk = min(PB, PLAN_BUCKETS / 2);
+  // the class of a sequence's item that does not come first: the last
+  // partition (r blocks) of a longer sequence, or the whole of a sequence of
+  // at most PB blocks
+  auto cls = [=](int nb) {
+    return nb > PB ? plan_bucket(nb % PB, PB, nbk) : nbk + plan_bucket(nb, PB + 1, nbk);
+  };
   slot[tid] = 0;
   __syncthreads();
   int nf = 0;
@@ -155,12 +164,12 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
     const int L0 = __ldg(p.context_lens + s);
     if (L0 < 0 || L0 > cap) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
     const int nb = (clamp_len(L0, cap) + Bs - 1) / Bs;
-    nf += nb / PB;
-    if (nb % PB) atomicAdd(&slot[plan_bucket(nb % PB, PB, nbk)], 1);
+    if (nb > PB) nf += nb / PB;
+    if (nb > 0 && (nb <= PB || nb % PB)) atomicAdd(&slot[cls(nb)], 1);
   }
   __syncthreads();
-  // block-wide exclusive scans: full partitions per thread, last partitions
-  // per length class (thread t holds class t)
+  // block-wide exclusive scans: first-group partitions per thread, the other
+  // items per class (thread t holds class t)
   const int np = slot[tid];
   int xf = nf, xp = np;
 #pragma unroll
@@ -191,9 +200,9 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   for (int s = s0; s < s1; ++s) {
     const int L = clamp_len(__ldg(p.context_lens + s), cap);
     const int nb = (L + Bs - 1) / Bs;
-    const int F = nb / PB;
+    const int F = nb > PB ? nb / PB : 0;
     for (int q = 0; q < F; ++q) p.items[fo++] = make_int2(s, q);
-    if (nb % PB) p.items[atomicAdd(&slot[plan_bucket(nb % PB, PB, nbk)], 1)] = make_int2(s, F);
+    if (nb > 0 && (nb <= PB || nb % PB)) p.items[atomicAdd(&slot[cls(nb)], 1)] = make_int2(s, F);
     if (L == 0) {   // nothing to attend to: zeros
       const size_t base = (size_t)s * p.num_q_heads * p.head_dim;
       for (int e = 0; e < p.num_q_heads * p.head_dim; ++e)
@@ -228,11 +237,11 @@ struct WarpLoads {
   const int32_t *trow;
 };
 
+// `item` = the work list's entry unit / num_hc.
 template <int B, int NCH, int CH, int NW>
 __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodeParams &p,
-                                                  unsigned unit, int w, int lane) {
+                                                  unsigned unit, int2 item, int w, int lane) {
   const int HC = p.num_hc;
-  const int2 item = __ldcg(p.items + unit / HC);
   const int hc = (int)(unit % HC);
   const int s = item.x, part = item.y;
   const int L0 = __ldg(p.context_lens + s);
@@ -323,10 +332,14 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   // everything above is local; the work list, the pool and q come from the
   // kernels before this one
   pdl_wait_predecessors();
-  if (tid == 0) {   // the first two units need no atomic (the counter starts past them)
-    s_int[0] = (int)blockIdx.x;
-    s_int[1] = (int)(blockIdx.x + gridDim.x);
-  }
+  // The first two units need no atomic (the counter starts past them), and
+  // their work-list entries are fetched together with the unit count (an
+  // entry past the list is read, from inside the array, but never used).
+  unsigned cur_unit = blockIdx.x;
+  unsigned nxt_unit = blockIdx.x + gridDim.x;
+  const size_t last_item = (size_t)p.num_seqs * p.max_parts - 1;
+  const int2 item0 = __ldcg(p.items + min((size_t)(cur_unit / HC), last_item));
+  const int2 item1 = __ldcg(p.items + min((size_t)(nxt_unit / HC), last_item));
   const unsigned total = __ldcg(p.ctrl + 1);
   __syncthreads();
 
@@ -343,11 +356,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   const int v_tok = ((lane >> 4) & 1) * 8 + (lane & 7);   // ldmatrix row for V (A, trans)
   const int v_chb = (lane >> 3) & 1;
 
-  unsigned cur_unit = (unsigned)s_int[0];
-  unsigned nxt_unit = (unsigned)s_int[1];
   WarpLoads cur, nxt;
-  if (cur_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(cur, p, cur_unit, w, lane);
-  if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, w, lane);
+  if (cur_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(cur, p, cur_unit, item0, w, lane);
+  if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, item1, w, lane);
 
   auto issue_chunk = [&](WarpLoads &wl) {
     const int u = wl.issued++;
@@ -708,7 +719,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
       }
     nxt_unit = (unsigned)s_int[qn];
     qn = qn == 2 ? 0 : qn + 1;
-    if (nxt_unit < total) decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, w, lane);
+    if (nxt_unit < total)
+      decode_unit_loads<B, C::NCH, C::CH, NW>(nxt, p, nxt_unit, __ldcg(p.items + nxt_unit / HC), w,
+                                              lane);
     top_up(cur_unit < total, nxt_unit < total);
   }
 
