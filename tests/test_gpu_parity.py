@@ -188,10 +188,11 @@ def test_workload_full_size_sampled(name):
         gh.assert_close_to_oracle(out16[seqs], ref.out, ATOL)
 
 
-@pytest.mark.parametrize("pt,append", [(512, False), (0, False), (512, True)])
+@pytest.mark.parametrize("pt,append", [(512, False), (0, False), (512, True), (128, False)])
 def test_longest_contexts_with_needles(pt, append):
     """Contexts far beyond the workloads': 131,072 tokens (256 partitions of
-    512, or a single unit streaming all of it), 65,537 (its new token opens a
+    512, 1,024 of 128 -- more records than the merge stages in shared memory
+    -- or a single unit streaming all of it), 65,537 (its new token opens a
     fresh block), one token only, and 4,097.  In KV head 0 one key of each
     long sequence is planted to score ~90 above the rest, deep inside the
     context, so that one far partition dominates the merge."""
