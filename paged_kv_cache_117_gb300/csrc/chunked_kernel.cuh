@@ -77,6 +77,7 @@ constexpr int CK_ST_MAX = 3;     // barrier slots per ring
 __host__ __device__ constexpr int ck_kst(bool convert) { return convert ? 2 : 3; }
 __host__ __device__ constexpr int ck_vst(bool convert) { return CK_STAGES - ck_kst(convert); }
 constexpr float CK_SLACK = 8.0f; // lazy rescale threshold (log2 domain)
+constexpr int CK_ORDER_MAX = 64; // sequences ranked by length at launch (at most)
 
 template <int D>
 struct ChunkCfg {
@@ -182,9 +183,31 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   const int pr_rev = id % p.num_qpairs;
   id /= p.num_qpairs;
   const int kvh = id % p.num_kv_heads;
-  const int s = id / p.num_kv_heads;
+  int s = id / p.num_kv_heads;                 // rank of the sequence in launch order
 
   pdl_wait_predecessors();
+  // Up to CK_ORDER_MAX sequences run longest context first (more keep index
+  // order): the CTAs of the longest contexts start in the first waves and
+  // the last wave holds short ones, so the SMs run out of work at nearly the
+  // same time.  Every CTA ranks the lengths the same way (ties by index).
+  if (p.num_seqs > 1 && p.num_seqs <= CK_ORDER_MAX) {
+    int *len_s = reinterpret_cast<int *>(sm + C::OFF_K);   // scratch: the K ring is still empty
+    int *ord_s = len_s + CK_ORDER_MAX;
+    for (int i = tid; i < p.num_seqs; i += NT) len_s[i] = p.context_lens[i];
+    __syncthreads();
+    for (int i = tid; i < p.num_seqs; i += NT) {
+      const int li = len_s[i];
+      int r = 0;
+      for (int j = 0; j < p.num_seqs; ++j) {
+        const int lj = len_s[j];
+        r += (lj > li) || (lj == li && j < i);
+      }
+      ord_s[r] = i;
+    }
+    __syncthreads();
+    s = ord_s[s];
+    fence_proxy_async_smem();   // the scratch is a TMA destination later
+  }
   const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
   const int n = q1 - q0;
   int L = p.context_lens[s];
