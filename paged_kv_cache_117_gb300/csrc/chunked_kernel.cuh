@@ -78,6 +78,7 @@ __host__ __device__ constexpr int ck_kst(bool convert) { return convert ? 2 : 3;
 __host__ __device__ constexpr int ck_vst(bool convert) { return CK_STAGES - ck_kst(convert); }
 constexpr float CK_SLACK = 8.0f; // lazy rescale threshold (log2 domain)
 constexpr int CK_ORDER_MAX = 64; // sequences ranked by length at launch (at most)
+constexpr int CK_SCAN_MAX = 2048;   // up to this many sequences the grid holds only real units
 
 template <int D>
 struct ChunkCfg {
@@ -121,6 +122,46 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+
+// In-place exclusive prefix sum of v[0..n) in shared memory by the whole
+// CTA of NT threads; returns the total.  red[0..NT/32) is scratch.  Every
+// thread must call it.
+template <int NT>
+__device__ __forceinline__ int cta_exclusive_scan(int *v, int n, int *red) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  constexpr int NWARP = NT / 32;
+  const int per = (n + NT - 1) / NT;
+  const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
+  int sum = 0;
+  for (int i = b0; i < b1; ++i) sum += v[i];
+  int x = sum;   // inclusive within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(FULL_MASK, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) red[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int t = lane < NWARP ? red[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, t, off);
+      if (lane >= off) t += y;
+    }
+    if (lane < NWARP) red[lane] = t;   // inclusive over warps
+  }
+  __syncthreads();
+  int run = x - sum + (wid ? red[wid - 1] : 0);
+  for (int i = b0; i < b1; ++i) {
+    const int c = v[i];
+    v[i] = run;
+    run += c;
+  }
+  const int total = red[NWARP - 1];
+  __syncthreads();
+  return total;
 }
 
 // Every lane of the warp waits; the result is the same on all lanes.
@@ -178,36 +219,84 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
 
   // ---- the unit: the query-tile pairs of one (sequence, KV head) are
   // adjacent in the grid, heaviest (last) pair first, so that they run at
-  // the same time and read each K/V tile from L2 rather than from HBM
-  int id = blockIdx.x;
-  const int pr_rev = id % p.num_qpairs;
-  id /= p.num_qpairs;
-  const int kvh = id % p.num_kv_heads;
-  int s = id / p.num_kv_heads;                 // rank of the sequence in launch order
-
+  // the same time and read each K/V tile from L2 rather than from HBM.
+  int s, kvh, pr_rev;
   pdl_wait_predecessors();
-  // Up to CK_ORDER_MAX sequences run longest context first (more keep index
-  // order): the CTAs of the longest contexts start in the first waves and
-  // the last wave holds short ones, so the SMs run out of work at nearly the
-  // same time.  Every CTA ranks the lengths the same way (ties by index).
-  if (p.num_seqs > 1 && p.num_seqs <= CK_ORDER_MAX) {
-    int *len_s = reinterpret_cast<int *>(sm + C::OFF_K);   // scratch: the K ring is still empty
-    int *ord_s = len_s + CK_ORDER_MAX;
-    for (int i = tid; i < p.num_seqs; i += NT) len_s[i] = p.context_lens[i];
-    __syncthreads();
-    for (int i = tid; i < p.num_seqs; i += NT) {
-      const int li = len_s[i];
-      int r = 0;
-      for (int j = 0; j < p.num_seqs; ++j) {
-        const int lj = len_s[j];
-        r += (lj > li) || (lj == li && j < i);
+  // Up to CK_ORDER_MAX sequences launch longest context first (ties by
+  // index; more keep index order): the CTAs of the longest contexts start in
+  // the first waves and the last wave holds short ones, so the SMs run out of
+  // work at nearly the same time.  Every CTA ranks the lengths the same way.
+  const int S = p.num_seqs;
+  const bool ranked = S > 1 && S <= CK_ORDER_MAX;
+  int *qs_s = reinterpret_cast<int *>(sm + C::OFF_K);   // scratch: the K ring is still empty
+  int *cnt_s = qs_s + CK_SCAN_MAX + 1;   // lengths, then units per launch slot, then offsets
+  int *ord_s = cnt_s + CK_SCAN_MAX;      // launch slot -> sequence
+  int *red = ord_s + CK_SCAN_MAX;        // [32] scan partials, [32] the slot found
+  auto rank_sequences = [&]() {
+    for (int i = tid; i < S; i += NT) {
+      int r = i;
+      if (ranked) {
+        const int li = cnt_s[i];
+        r = 0;
+        for (int j = 0; j < S; ++j) {
+          const int lj = cnt_s[j];
+          r += (lj > li) || (lj == li && j < i);
+        }
       }
       ord_s[r] = i;
     }
+  };
+  if (p.compact) {
+    // The grid holds only units that exist (many sequences have fewer query
+    // tiles than the longest): every CTA lists the sequences' unit counts
+    // (query-tile pairs x KV heads; a sequence whose query range is invalid
+    // keeps one unit, which flags it) in launch order, takes the exclusive
+    // sum and finds its own unit.
+    const int TQ = p.tile_tokens;
+    for (int i = tid; i <= S; i += NT) qs_s[i] = p.query_start[i];
+    for (int i = tid; i < S; i += NT) cnt_s[i] = p.context_lens[i];
     __syncthreads();
-    s = ord_s[s];
-    fence_proxy_async_smem();   // the scratch is a TMA destination later
+    rank_sequences();
+    __syncthreads();
+    for (int r = tid; r < S; r += NT) {
+      const int q = ord_s[r];
+      const int a = qs_s[q], b = qs_s[q + 1], n = b - a;
+      const bool valid = a >= 0 && n >= 0 && b <= p.num_tokens && n <= p.max_query_len;
+      cnt_s[r] = (!valid ? 1 : ((n + TQ - 1) / TQ + 1) / 2) * p.num_kv_heads;
+    }
+    if (tid == 0) red[32] = -1;
+    __syncthreads();
+    const int total = cta_exclusive_scan<NT>(cnt_s, S, red);
+    const int b = (int)blockIdx.x;
+    for (int r = tid; r < S; r += NT)
+      if (cnt_s[r] <= b && b < (r + 1 < S ? cnt_s[r + 1] : total)) red[32] = r;
+    __syncthreads();
+    const int r = red[32];
+    // (the grid is an upper bound; it falls short only when query ranges
+    // overlap, which no valid batch has)
+    if (b == 0 && tid == 0 && total > (int)gridDim.x) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
+    if (b >= total || r < 0) return;
+    s = ord_s[r];
+    const int units = (r + 1 < S ? cnt_s[r + 1] : total) - cnt_s[r];
+    const int npairs = units / p.num_kv_heads;
+    kvh = (b - cnt_s[r]) / npairs;
+    pr_rev = (b - cnt_s[r]) % npairs;
+  } else {
+    // every (sequence, KV head, pair) slot of the longest query range
+    int id = blockIdx.x;
+    pr_rev = id % p.num_qpairs;
+    id /= p.num_qpairs;
+    kvh = id % p.num_kv_heads;
+    s = id / p.num_kv_heads;               // rank of the sequence in launch order
+    if (ranked) {
+      for (int i = tid; i < S; i += NT) cnt_s[i] = p.context_lens[i];
+      __syncthreads();
+      rank_sequences();
+      __syncthreads();
+      s = ord_s[s];
+    }
   }
+  fence_proxy_async_smem();   // the scratch is a TMA destination later
   const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
   const int n = q1 - q0;
   int L = p.context_lens[s];
@@ -801,11 +890,22 @@ cudaError_t launch_chunked_p(const CUtensorMap &qmap, const CUtensorMap &kmap,
   static_assert(C::SMEM <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long units = (long long)p.num_qpairs * p.num_seqs * p.num_kv_heads;
+  // every (sequence, KV head, pair of query tiles) of the longest query
+  // range; or, when that is smaller and there are at most CK_SCAN_MAX
+  // sequences, only the units that exist (compact), bounded by
+  // S + ceil(tokens / 2 tiles) pairs per KV head (a sequence of n > 0 queries
+  // has ceil(ceil(n / TQ) / 2) <= n / (2 TQ) + 1 pairs; an invalid one keeps one)
+  ChunkedParams pc = p;
+  long long units = (long long)p.num_qpairs * p.num_seqs * p.num_kv_heads;
+  const long long bound =
+      ((long long)p.num_seqs + (p.num_tokens + 2LL * p.tile_tokens - 1) / (2LL * p.tile_tokens)) *
+      p.num_kv_heads;
+  pc.compact = p.num_seqs <= CK_SCAN_MAX && bound < units ? 1 : 0;
+  if (pc.compact) units = bound;
   if (units <= 0) return cudaSuccess;
   constexpr int NT = ck_threads(P16 && std::is_same<T, __nv_bfloat16>::value);
   return launch_pdl(kern, dim3((unsigned)units), dim3(NT), (size_t)C::SMEM, stream, qmap,
-                    kmap, vmap, p);
+                    kmap, vmap, pc);
 }
 
 template <typename T, int D, int B>

@@ -101,6 +101,7 @@ struct ChunkedParams {
   int tile_tokens;
   int num_qtiles;                // ceil(max_query_len / tile_tokens)
   int num_qpairs;                // ceil(num_qtiles / 2): query tiles go two to a CTA
+  int compact = 0;               // the grid lists only existing units (set at launch)
   int p_format;                  // pkv_p_format
   int max_query_len;
   int num_blocks;
