@@ -1,0 +1,70 @@
+"""The benchmark's workload selection on CPU: resizing a decode workload with
+--seqs / --context keeps its heads, dtype, block size and partition, sizes
+the pool and the table width for every sequence, names the result so that no
+committed profile applies to it, and refuses the workloads whose sequences
+share blocks or carry several query rows."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from paged_kv_cache_117_gb300 import workloads as wl  # noqa: E402
+
+
+class Args:
+    def __init__(self, workload="llama8b", seqs=None, context=None):
+        self.workload, self.seqs, self.context = workload, seqs, context
+
+
+def test_named_workload_is_unchanged():
+    assert bench.select_workload(Args()) is wl.LLAMA8B
+
+
+def test_fixed_batch_shape():
+    w = bench.select_workload(Args(seqs=64, context=4096))
+    base = wl.LLAMA8B
+    assert (w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.dtype,
+            w.partition_tokens) == (base.num_q_heads, base.num_kv_heads, base.head_dim,
+                                    base.block_size, base.dtype, base.partition_tokens)
+    lens, tables, width = bench.build_metadata(w)
+    assert lens == [4096] * 64
+    assert width == 4096 // 16
+    assert all(len(t) == 256 for t in tables)
+    # every block is distinct and inside the pool
+    flat = [b for t in tables for b in t]
+    assert len(set(flat)) == len(flat) and max(flat) < w.num_blocks
+    assert w.name not in bench.TABLE_WIDTH_TOKENS
+    assert bench.measured_traffic(w.name, w.partition_tokens, kv_write="append") is None
+
+
+def test_more_sequences_keep_the_distribution():
+    w = bench.select_workload(Args(seqs=32))
+    assert w.lens_kind == wl.LLAMA8B.lens_kind and w.num_seqs == 32
+    lens, tables, width = bench.build_metadata(w)
+    assert len(lens) == 32 and max(lens) <= width * w.block_size
+
+
+def test_bytes_scale_with_the_batch():
+    small = bench.select_workload(Args(seqs=8, context=1024))
+    big = bench.select_workload(Args(seqs=16, context=1024))
+    b_small = bench.algorithmic_bytes(small, *bench.build_metadata(small), 768, 2)
+    b_big = bench.algorithmic_bytes(big, *bench.build_metadata(big), 768, 2)
+    assert b_big["kv"] == 2 * b_small["kv"]
+    assert b_small["kv"] == 8 * 1024 * small.num_kv_heads * small.head_dim * 2 * 2
+
+
+@pytest.mark.parametrize("name", ["shared", "beam", "prefill", "prefix"])
+def test_other_workloads_refuse_resizing(name):
+    with pytest.raises(SystemExit):
+        bench.select_workload(Args(workload=name, seqs=4, context=1024))
+
+
+def test_sizes_must_be_positive():
+    with pytest.raises(SystemExit):
+        bench.select_workload(Args(seqs=0, context=1024))
+    with pytest.raises(SystemExit):
+        bench.select_workload(Args(seqs=4, context=0))
