@@ -257,7 +257,12 @@ typedef enum {
  * skipped (its rows are left untouched) and flagged PKV_FLAG_LEN_RANGE; L_s
  * past the table is clamped and flagged; bad block ids are read as zeros and
  * flagged PKV_FLAG_BLOCK_RANGE.  No workspace: one launch, one CTA per
- * (two query tiles of 128 / G tokens each, sequence, KV head).
+ * (two query tiles of 128 / G tokens each, sequence, KV head); with up to
+ * 2,048 sequences of which some have fewer query tiles than the longest, the
+ * grid holds only the units that exist, which query ranges that overlap
+ * (against the non-decreasing rule above) can exceed: then some units are not
+ * run and PKV_FLAG_LEN_RANGE is set.  Up to 64 sequences launch longest
+ * context first (the order changes no result).
  */
 pkv_status paged_attention_chunked(
     void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
