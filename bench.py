@@ -930,7 +930,37 @@ def run_native_chunked(a, world, rank, local):
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
         "cpu_baseline": cpu,
+        **({"host_manager": prefix_manager_cost(w)} if w.lens_kind == "prefix" else {}),
     }
+
+
+def prefix_manager_cost(w, rounds=20):
+    """Host time of the library's prefix-cache manager per request of the
+    prefix workload: the prompt's lookup (the chained SHA-256 key of each full
+    block, then the key map), the append of its own tokens and its release,
+    through the Python binding, on a cache that holds the system prompts."""
+    import paged_kv_cache_117_gb300 as pkv
+    plan = wl.prefix_plan(w)
+    pc = pkv.PrefixCache(w.num_blocks, w.block_size, wl.free_block_order(w))
+    for i, sysp in enumerate(plan.systems):
+        sid = len(plan.prompts) + i
+        warm = sysp + [0]
+        c = pc.add_sequence(sid, warm)
+        pc.append(sid, warm[c:])
+        pc.free_sequence(sid)
+    prompts = [torch.tensor(p_, dtype=torch.int32) for p_ in plan.prompts]
+    t0 = time.perf_counter()
+    for _ in range(rounds):
+        for r, p_ in enumerate(prompts):
+            c = pc.add_sequence(r, p_)
+            pc.append(r, p_[c:])
+        for r in range(len(prompts)):
+            pc.free_sequence(r)
+    us = (time.perf_counter() - t0) / (rounds * len(prompts)) * 1e6
+    return {"us_per_request": round(us, 1), "requests": len(prompts),
+            "prompt_tokens": len(plan.prompts[0]), "cpu": cpu_model(),
+            "what": "lookup + append + free per request, host C++ through the binding; after "
+                    "the first round the questions' own blocks are cached too"}
 
 
 def run_reference(a, world, rank, local):

@@ -416,6 +416,10 @@ class BlockManager:
 
 
 def _i32(xs) -> torch.Tensor:
+    """A host int32 copy of a tensor or a sequence of ints (for the host
+    managers' C calls)."""
+    if isinstance(xs, torch.Tensor):
+        return xs.detach().to(device="cpu", dtype=torch.int32).contiguous()
     return torch.as_tensor(list(xs), dtype=torch.int32).contiguous()
 
 
