@@ -352,7 +352,7 @@ class BlockManager:
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         order = None
         if free_order is not None:
-            order = torch.as_tensor(list(free_order), dtype=torch.int32).contiguous()
+            order = _host(free_order, torch.int32)
             if order.numel() != num_blocks:
                 raise ValueError("free_order must list every block once")
         self._order = order
@@ -379,7 +379,7 @@ class BlockManager:
     def append(self, seqs):
         """Next-token slots of ``seqs`` (in order) and the copy-on-write pairs
         that must run first: (int64 [n] slots, int64 [P, 2] pairs), CPU."""
-        ids = torch.as_tensor(list(seqs), dtype=torch.int64).contiguous()
+        ids = _host(seqs, torch.int64)
         n = ids.numel()
         slots = torch.empty(n, dtype=torch.int64)
         pairs = torch.empty((max(n, 1), 2), dtype=torch.int64)
@@ -415,12 +415,16 @@ class BlockManager:
         return int(self._lib.pkv_bm_refcount(self._h, int(block)))
 
 
-def _i32(xs) -> torch.Tensor:
-    """A host int32 copy of a tensor or a sequence of ints (for the host
-    managers' C calls)."""
+def _host(xs, dtype) -> torch.Tensor:
+    """A contiguous host copy of a tensor or a sequence of ints, in `dtype`
+    (for the host managers' C calls)."""
     if isinstance(xs, torch.Tensor):
-        return xs.detach().to(device="cpu", dtype=torch.int32).contiguous()
-    return torch.as_tensor(list(xs), dtype=torch.int32).contiguous()
+        return xs.detach().to(device="cpu", dtype=dtype).contiguous()
+    return torch.as_tensor(list(xs), dtype=dtype).contiguous()
+
+
+def _i32(xs) -> torch.Tensor:
+    return _host(xs, torch.int32)
 
 
 def sha256(data: bytes) -> bytes:
