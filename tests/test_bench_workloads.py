@@ -68,3 +68,10 @@ def test_sizes_must_be_positive():
         bench.select_workload(Args(seqs=0, context=1024))
     with pytest.raises(SystemExit):
         bench.select_workload(Args(seqs=4, context=0))
+
+
+def test_prefix_manager_cost_is_reported():
+    cost = bench.prefix_manager_cost(wl.PREFIX, rounds=1)
+    assert cost["requests"] == wl.PREFIX.num_seqs
+    assert cost["prompt_tokens"] == 2048 + 256
+    assert 0 < cost["us_per_request"] < 1e6
