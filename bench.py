@@ -143,11 +143,37 @@ def width_tokens(w):
 # ---------------------------------------------------------------------------
 # workload and its algorithmic bytes
 
-def build_metadata(w):
-    lens = wl.context_lens(w)
-    tables = wl.scatter_block_tables(lens, w.block_size, wl.free_block_order(w))
+def build_metadata(w, manager="native"):
+    """Decode state of independent sequences, built by a block manager whose
+    free queue is the workload's seeded permutation (so each sequence's
+    blocks are scattered over the pool): every sequence's earlier tokens,
+    then this step's token of every sequence.  ``manager``: "native" (the
+    library's pkv_bm_*) or "oracle" (the reference arm's, no library call).
+    Returns lens, tables, width and the step's slot per sequence (int64,
+    CPU), as the manager assigned them."""
+    lens0 = wl.context_lens(w)
+    S = len(lens0)
+    if manager == "native":
+        import paged_kv_cache_117_gb300 as pkv
+        bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+        for s, L in enumerate(lens0):
+            bm.add_sequence(s)
+            if L > 1:
+                bm.append_tokens(s, L - 1)
+        slots, pairs = bm.append(range(S))
+        assert pairs.shape[0] == 0
+        tables, lens = zip(*(bm.table(s) for s in range(S)))
+    else:
+        from oracle.block_manager import BlockManager
+        bm = BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+        for s, L in enumerate(lens0):
+            bm.add_sequence(s)
+            bm.append_tokens(s, max(0, L - 1))
+        slots = torch.tensor([bm.append(s)[0] for s in range(S)], dtype=torch.int64)
+        tables, lens = [bm.tables[s] for s in range(S)], [bm.lens[s] for s in range(S)]
+    assert list(lens) == lens0
     width = -(-width_tokens(w) // w.block_size)
-    return lens, tables, width
+    return lens0, [list(t) for t in tables], width, slots
 
 
 def build_shared_step(w):
@@ -540,12 +566,10 @@ def run_native(a, world, rank, local):
         lens, tables, width, slots_cpu, pairs_cpu, hist = build_beam_step(w)
         replay_beam_history(w, k, v, hist, dev)
     else:
-        lens, tables, width = build_metadata(w)
+        lens, tables, width, slots_cpu = build_metadata(w)
         pairs_cpu = torch.zeros((0, 2), dtype=torch.int64)
     tab_cpu = wl.pad_tables(tables, width)
     lens_cpu = torch.tensor(lens, dtype=torch.int32)
-    if w.lens_kind not in SHARING:
-        slots_cpu = pkv.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size)
     q, key, value = wl.make_step_inputs(w, dev)
     tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
     pairs = pairs_cpu.to(dev)
@@ -590,11 +614,6 @@ def run_native(a, world, rank, local):
 
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
-
-    if fused:   # the call derives each new token's slot from the tables
-        B = w.block_size
-        for s_, (t_, L_) in enumerate(zip(tables, lens)):
-            assert int(slots_cpu[s_]) == (t_[(L_ - 1) // B] * B + (L_ - 1) % B if L_ else -1)
 
     def attend(o, ql, keyl, vall, kl, vl, tb, ln, wsl):
         if fused:
@@ -938,9 +957,17 @@ def prefix_manager_cost(w, rounds=20):
     """Host time of the library's prefix-cache manager per request of the
     prefix workload: the prompt's lookup (the chained SHA-256 key of each full
     block, then the key map), the append of its own tokens and its release,
-    through the Python binding, on a cache that holds the system prompts."""
+    through the Python binding, on a cache that holds the system prompts.
+
+    Two costs are reported.  ``miss``: every round brings requests with fresh
+    (seeded) questions, so each request finds only its system prompt cached
+    and allocates blocks for its own tokens, evicting cached blocks of earlier
+    rounds from the free queue.  ``hit``: the same requests again right after,
+    when their question blocks are cached too.  ``us_per_request`` is the miss
+    cost (a new request's)."""
     import paged_kv_cache_117_gb300 as pkv
     plan = wl.prefix_plan(w)
+    n_sys, _, q_len = w.lens_args
     pc = pkv.PrefixCache(w.num_blocks, w.block_size, wl.free_block_order(w))
     for i, sysp in enumerate(plan.systems):
         sid = len(plan.prompts) + i
@@ -948,19 +975,41 @@ def prefix_manager_cost(w, rounds=20):
         c = pc.add_sequence(sid, warm)
         pc.append(sid, warm[c:])
         pc.free_sequence(sid)
-    prompts = [torch.tensor(p_, dtype=torch.int32) for p_ in plan.prompts]
-    t0 = time.perf_counter()
-    for _ in range(rounds):
+    systems = [torch.tensor(sp, dtype=torch.int32) for sp in plan.systems]
+    g = torch.Generator().manual_seed(w.seed + 7000)
+    R = len(plan.prompts)
+
+    def admit(prompts):
+        t0 = time.perf_counter()
+        cached = 0
         for r, p_ in enumerate(prompts):
             c = pc.add_sequence(r, p_)
             pc.append(r, p_[c:])
-        for r in range(len(prompts)):
+            cached += c
+        for r in range(R):
             pc.free_sequence(r)
-    us = (time.perf_counter() - t0) / (rounds * len(prompts)) * 1e6
-    return {"us_per_request": round(us, 1), "requests": len(prompts),
-            "prompt_tokens": len(plan.prompts[0]), "cpu": cpu_model(),
-            "what": "lookup + append + free per request, host C++ through the binding; after "
-                    "the first round the questions' own blocks are cached too"}
+        return time.perf_counter() - t0, cached
+
+    t_miss = t_hit = 0.0
+    c_miss = c_hit = 0
+    for _ in range(rounds):
+        qs = torch.randint(0, 32000, (R, q_len), generator=g, dtype=torch.int32)
+        prompts = [torch.cat([systems[r % n_sys], qs[r]]) for r in range(R)]
+        dt, c = admit(prompts)
+        t_miss, c_miss = t_miss + dt, c_miss + c
+        dt, c = admit(prompts)
+        t_hit, c_hit = t_hit + dt, c_hit + c
+    miss = t_miss / (rounds * R) * 1e6
+    hit = t_hit / (rounds * R) * 1e6
+    return {"us_per_request": round(miss, 1), "us_per_request_miss": round(miss, 1),
+            "us_per_request_hit": round(hit, 1), "requests": R,
+            "prompt_tokens": len(plan.prompts[0]),
+            "cached_tokens_per_request_miss": c_miss // (rounds * R),
+            "cached_tokens_per_request_hit": c_hit // (rounds * R), "cpu": cpu_model(),
+            "what": "lookup + append + free per request, host C++ through the binding; miss: "
+                    "fresh questions (only the system prompt cached; blocks allocated and "
+                    "older cached blocks evicted), hit: the same requests again (all full "
+                    "blocks cached); us_per_request is the miss cost"}
 
 
 def run_reference(a, world, rank, local):
@@ -973,7 +1022,7 @@ def run_reference(a, world, rank, local):
     elif w.lens_kind == "beam":
         lens, tables, width, slot_t, _, _ = build_beam_step(w)
     else:
-        lens, tables, width = build_metadata(w)
+        lens, tables, width, slot_t = build_metadata(w, manager="oracle")
     # inputs with the same distributions, generated on the CPU for just the
     # blocks the sample reads (no GPU needed)
     nseq = max(1, min(w.num_seqs, 4))
@@ -983,11 +1032,7 @@ def run_reference(a, world, rank, local):
     kc = torch.randn(shape, generator=g).to(w.dtype)
     vc = torch.randn(shape, generator=g).to(w.dtype)
     q, key, value = wl.make_step_inputs(w, "cpu")
-    tab_cpu = wl.pad_tables(tables, width)
-    lens_cpu = torch.tensor(lens, dtype=torch.int32)
-    import paged_kv_cache_117_gb300.binding as bnd
-    slots = (slot_t.tolist() if w.lens_kind in SHARING
-             else bnd.decode_slot_mapping(tab_cpu, lens_cpu, w.block_size).tolist())
+    slots = slot_t.tolist()
     times, nbytes, threads = [], 0, torch.get_num_threads()
     for i in range(max(3, a.warmup) + a.steps):
         dt, b, threads = oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value,

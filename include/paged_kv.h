@@ -86,9 +86,10 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 /*
  * paged_kv_write -- store new keys/values into their slots.
  *
- * "The key and value are written to its assigned block and offset"
- * ("PagedAttention", section 5); the write kernel is one fused launch for all
- * tokens ("PagedAttention and vLLM ...", Step 5, "Write").
+ * Each new token's key and value rows are stored at the block and offset
+ * that its slot names ("PagedAttention", section 5); one launch writes the
+ * rows of every token of the step ("PagedAttention and vLLM ...", Step 5,
+ * "Write").
  *
  *   key, value    [num_tokens, num_kv_heads, head_dim], cache dtype
  *   k_cache,
@@ -110,8 +111,8 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache,
 /*
  * paged_block_copy -- batched copy-on-write block copy.
  *
- * "Copy-on-write can trigger many small block copies in one step, so one
- * kernel batches them" ("PagedAttention and vLLM ...", Step 5, "Copy").  For
+ * A step's copy-on-write may ask for many small block copies; they all run in
+ * a single launch ("PagedAttention and vLLM ...", Step 5, "Copy").  For
  * every pair, all block_size slots of block src are copied to block dst, in
  * k_cache and in v_cache, bit-exactly, in one launch.
  *
@@ -227,9 +228,8 @@ typedef enum {
  * chunks of prompts (chunked prefill) and decode tokens in one batch.
  *
  * "Paging the KV Cache Like an OS" (continuous batching; chunked prefill): a
- * long prompt is split into chunks processed over several passes, each
- * filling a few blocks allocated on demand, interleaved with other
- * sequences' decode steps.  Sequence s contributes the n_s = query_start[s+1]
+ * prompt is prefilled a piece at a time over several steps, each piece
+ * filling blocks taken on demand, alongside other sequences' decode tokens.  Sequence s contributes the n_s = query_start[s+1]
  * - query_start[s] query rows q[query_start[s] .. query_start[s+1]-1], its
  * LAST n_s positions: with L_s = context_lens[s] (which counts them), row i
  * sits at position p = L_s - n_s + i and attends to positions 0..p of its own
@@ -309,8 +309,11 @@ size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
  *    exceeds PKV_NOALLOC_SCRATCH_BYTES returns PKV_ERR_WORKSPACE before any
  *    CUDA call.
  *  - Set-up: the first call on a device (with that device current) looks up
- *    the array's device address once; make that first call before any stream
- *    capture.
+ *    the array's device address once and keeps it for the life of the
+ *    process; make that first call before any stream capture.  The kept
+ *    address is not refreshed: after cudaDeviceReset on a device this entry
+ *    point must not be called on that device again in the same process (the
+ *    module may be reloaded elsewhere and the kept address would be stale).
  *  - Sharing: every call on a device uses the same array, which keeps the
  *    last call's contents (the call resets what must start at zero).  Calls
  *    that overlap in time on one device race; order them on one stream.

@@ -12,10 +12,11 @@ Follows the pages step by step:
   2.4 free queue).
 * Forking a sequence copies its block table and raises each block's reference
   count ("PagedAttention and vLLM ...", Step 4, beam search paragraph).
-* Writing into a block whose count is above one first copies it to a fresh
-  block, points the writer's table at the copy and lowers the original's count;
-  a writer that finds the count at one writes in place ("PagedAttention and
-  vLLM ...", Step 4, parallel sampling paragraph).
+* A write into a block that others still hold (count above one) goes to a
+  fresh copy of it: the writer's table entry is switched to the copy and the
+  shared block's count drops by one; a writer that holds the block alone
+  (count one) writes straight into it ("PagedAttention and vLLM ...", Step 4,
+  parallel sampling paragraph).
 
 The manager tracks metadata only.  The copies it asks for are returned as
 (src, dst) pairs; ``paged_ops.copy_blocks`` moves the bytes.

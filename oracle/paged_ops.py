@@ -27,10 +27,9 @@ import torch
 
 def write_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, key: torch.Tensor,
              value: torch.Tensor, slot_mapping: Sequence[int]) -> None:
-    """Store token t's key/value rows at (slot // B, slot % B), in place.
-
-    "The key and value are written to its assigned block and offset" --
-    "PagedAttention" (tensortonic), section 5.
+    """Store token t's key/value rows at (slot // B, slot % B), in place:
+    the block and offset the token's slot names ("PagedAttention"
+    (tensortonic), section 5).
     """
     B = k_cache.shape[1]
     for t, slot in enumerate(int(x) for x in slot_mapping):
@@ -45,9 +44,9 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
                 pairs: Iterable[Tuple[int, int]]) -> None:
     """Copy every slot of block src to block dst, keys and values, in place.
 
-    The copy-on-write copy: "allocates a new block, copies the existing tokens
-    into it" -- "PagedAttention and vLLM ...", Step 4.  The whole block is
-    copied (all block_size slots).
+    The copy-on-write copy: the writer takes a fresh block and the tokens
+    held so far are copied into it ("PagedAttention and vLLM ...", Step 4).
+    The whole block is copied (all block_size slots).
     """
     for src, dst in pairs:
         k_cache[int(dst)] = k_cache[int(src)].clone()

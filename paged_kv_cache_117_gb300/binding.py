@@ -330,19 +330,6 @@ def read_device_flags(clear: bool = True, stream=None) -> int:
     return int(v.value)
 
 
-def decode_slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor,
-                        block_size: int) -> torch.Tensor:
-    """Slot of each sequence's newest token (position L_s - 1):
-    table[s][(L_s - 1) // B] * B + (L_s - 1) % B; -1 for empty sequences.
-    Host-side helper for building a decode step's slot_mapping."""
-    lens = context_lens.to(torch.int64).cpu()
-    tabs = block_tables.to(torch.int64).cpu()
-    pos = (lens - 1).clamp(min=0)
-    blk = tabs.gather(1, (pos // block_size).unsqueeze(1)).squeeze(1)
-    slots = blk * block_size + pos % block_size
-    return torch.where(lens > 0, slots, torch.full_like(slots, -1))
-
-
 class BlockManager:
     """The library's host-side block manager (pkv_bm_* in the C ABI): block
     allocation, reference counts and copy-on-write for one pool."""
@@ -417,10 +404,24 @@ class BlockManager:
 
 def _host(xs, dtype) -> torch.Tensor:
     """A contiguous host copy of a tensor or a sequence of ints, in `dtype`
-    (for the host managers' C calls)."""
+    (for the host managers' C calls).  A tensor must hold integers that fit
+    `dtype`: a float, complex or bool tensor, or a value out of range, raises
+    ValueError, as the sequence path does (a value that wrapped would, for
+    example, give two different token streams the same block key)."""
     if isinstance(xs, torch.Tensor):
-        return xs.detach().to(device="cpu", dtype=dtype).contiguous()
-    return torch.as_tensor(list(xs), dtype=dtype).contiguous()
+        t = xs.detach().to(device="cpu")
+        if t.dtype.is_floating_point or t.dtype.is_complex or t.dtype == torch.bool:
+            raise ValueError(f"integer tensor expected, got {t.dtype}")
+        if t.numel():
+            info = torch.iinfo(dtype)
+            lo, hi = int(t.min()), int(t.max())
+            if lo < info.min or hi > info.max:
+                raise ValueError(f"value out of range for {dtype}: [{lo}, {hi}]")
+        return t.to(dtype=dtype).contiguous()
+    try:
+        return torch.as_tensor(list(xs), dtype=dtype).contiguous()
+    except (RuntimeError, TypeError) as e:
+        raise ValueError(f"integers that fit {dtype} expected: {e}") from None
 
 
 def _i32(xs) -> torch.Tensor:

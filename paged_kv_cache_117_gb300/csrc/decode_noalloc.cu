@@ -15,7 +15,9 @@
 // Set-up: the first call on a device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress and caches it; later calls
 // on that device reuse it.  Make that first call before any stream capture.
-// Nothing here allocates memory.
+// The cached address is never refreshed, so a process that calls
+// cudaDeviceReset on a device must not call this entry point on that device
+// again.  Nothing here allocates memory.
 //
 // The array is shared by every call on a device and keeps the last call's
 // contents; the attention pass resets what must start at zero itself.  Calls

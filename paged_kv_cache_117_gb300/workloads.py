@@ -230,21 +230,6 @@ def pad_tables(tables: Sequence[Sequence[int]], width: Optional[int] = None,
     return out
 
 
-def scatter_block_tables(lens: Sequence[int], block_size: int,
-                         order: Sequence[int]) -> List[List[int]]:
-    """Hand each sequence ceil(L_s / block_size) blocks, in sequence order,
-    from the front of ``order`` (the seeded free-block permutation): the
-    random scatter of blocks over the pool that the workloads call for."""
-    tables, pos = [], 0
-    for L in lens:
-        nb = -(-int(L) // block_size)
-        if pos + nb > len(order):
-            raise ValueError("pool too small for these lengths")
-        tables.append([int(b) for b in order[pos:pos + nb]])
-        pos += nb
-    return tables
-
-
 def chunk_plan(w: Workload):
     """(prior tokens, this step's query tokens) per sequence of a chunked
     prefill workload."""

@@ -30,8 +30,8 @@ def test_fixed_batch_shape():
     assert (w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.dtype,
             w.partition_tokens) == (base.num_q_heads, base.num_kv_heads, base.head_dim,
                                     base.block_size, base.dtype, base.partition_tokens)
-    lens, tables, width = bench.build_metadata(w)
-    assert lens == [4096] * 64
+    lens, tables, width, slots = bench.build_metadata(w)
+    assert lens == [4096] * 64 and slots.shape == (64,)
     assert width == 4096 // 16
     assert all(len(t) == 256 for t in tables)
     # every block is distinct and inside the pool
@@ -44,15 +44,15 @@ def test_fixed_batch_shape():
 def test_more_sequences_keep_the_distribution():
     w = bench.select_workload(Args(seqs=32))
     assert w.lens_kind == wl.LLAMA8B.lens_kind and w.num_seqs == 32
-    lens, tables, width = bench.build_metadata(w)
+    lens, tables, width, _ = bench.build_metadata(w)
     assert len(lens) == 32 and max(lens) <= width * w.block_size
 
 
 def test_bytes_scale_with_the_batch():
     small = bench.select_workload(Args(seqs=8, context=1024))
     big = bench.select_workload(Args(seqs=16, context=1024))
-    b_small = bench.algorithmic_bytes(small, *bench.build_metadata(small), 768, 2)
-    b_big = bench.algorithmic_bytes(big, *bench.build_metadata(big), 768, 2)
+    b_small = bench.algorithmic_bytes(small, *bench.build_metadata(small)[:3], 768, 2)
+    b_big = bench.algorithmic_bytes(big, *bench.build_metadata(big)[:3], 768, 2)
     assert b_big["kv"] == 2 * b_small["kv"]
     assert b_small["kv"] == 8 * 1024 * small.num_kv_heads * small.head_dim * 2 * 2
 
@@ -63,6 +63,25 @@ def test_other_workloads_refuse_resizing(name):
         bench.select_workload(Args(workload=name, seqs=4, context=1024))
 
 
+@pytest.mark.parametrize("name", ["tiny", "opt13b"])
+def test_decode_state_from_the_native_manager_matches_the_oracle_manager(name):
+    """The benchmark's decode state (tables, lengths and the step's slots)
+    comes from the library's block manager through the C ABI; the oracle's
+    manager, fed the same free queue and the same appends, assigns the same
+    blocks and slots."""
+    w = wl.scaled(wl.WORKLOADS[name], 16, 1024) if name != "tiny" else wl.TINY
+    native = bench.build_metadata(w, manager="native")
+    ref = bench.build_metadata(w, manager="oracle")
+    assert native[:3] == ref[:3]
+    assert native[3].tolist() == ref[3].tolist()
+    # tiny: lengths 1, 6, 9, 17 in 4-token blocks; 1, 9 and 17 open a fresh block
+    if name == "tiny":
+        tables, slots = native[1], native[3].tolist()
+        for s, L in enumerate(native[0]):
+            assert len(tables[s]) == -(-L // 4)
+            assert slots[s] // 4 == tables[s][-1] and slots[s] % 4 == (L - 1) % 4
+
+
 def test_sizes_must_be_positive():
     with pytest.raises(SystemExit):
         bench.select_workload(Args(seqs=0, context=1024))
@@ -71,7 +90,13 @@ def test_sizes_must_be_positive():
 
 
 def test_prefix_manager_cost_is_reported():
-    cost = bench.prefix_manager_cost(wl.PREFIX, rounds=1)
+    cost = bench.prefix_manager_cost(wl.PREFIX, rounds=2)
     assert cost["requests"] == wl.PREFIX.num_seqs
     assert cost["prompt_tokens"] == 2048 + 256
-    assert 0 < cost["us_per_request"] < 1e6
+    assert 0 < cost["us_per_request"] == cost["us_per_request_miss"] < 1e6
+    assert 0 < cost["us_per_request_hit"] < 1e6
+    # a new request finds its system prompt cached (128 full blocks of 16);
+    # the same request again finds every full block cached but the one that
+    # holds its last token, which is always recomputed
+    assert cost["cached_tokens_per_request_miss"] == 2048
+    assert cost["cached_tokens_per_request_hit"] == 2048 + 256 - 16

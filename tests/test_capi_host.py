@@ -185,20 +185,3 @@ def test_copy_validation(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="CUDA library not found"):
         pkv.load(str(tmp_path / "missing.so"))
-
-
-def test_decode_slot_mapping_matches_oracle_manager():
-    import torch
-    from oracle.block_manager import BlockManager
-    from paged_kv_cache_117_gb300 import workloads as wl
-    bm = BlockManager(64, 4, free_order=wl.free_block_order(wl.TINY))
-    want = []
-    for s, L in enumerate([1, 6, 9, 17]):
-        bm.add_sequence(s)
-        bm.append_tokens(s, L - 1)
-        want.append(bm.append(s)[0])
-    tables = wl.pad_tables([bm.tables[s] for s in range(4)])
-    lens = torch.tensor([1, 6, 9, 17], dtype=torch.int32)
-    got = pkv.decode_slot_mapping(tables, lens, 4)
-    assert got.tolist() == want
-    assert pkv.decode_slot_mapping(tables, torch.tensor([0, 6, 9, 17], dtype=torch.int32), 4)[0] == -1

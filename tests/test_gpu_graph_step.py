@@ -2,7 +2,7 @@
 every layer -- captured in one CUDA graph and replayed, against the oracle.
 
 Every layer has its own K/V pool but the same block tables, slot mapping and
-copy pairs: one block id names the same slot range in every layer's cache
+copy pairs: a block id stands for the same slot range in each layer's cache
 ("PagedAttention and vLLM: Paging the KV Cache Like an OS", 'How much can still
 be wasted').  The step is idempotent (same copies, same writes), so replaying
 the graph twice must leave the same pools and outputs as one eager pass."""

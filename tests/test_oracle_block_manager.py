@@ -62,7 +62,7 @@ def test_request_a_walkthrough():
     bm.append(0)                               # token 49
     assert len(bm.tables[0]) == 4 and g["token_49_needs_new_block"]
     before = bm.num_used_blocks()
-    bm.free_sequence(0)                        # "When A ends, its blocks go back"
+    bm.free_sequence(0)                        # a finished request returns its blocks
     assert bm.num_used_blocks() == before - 4 == 0
 
 

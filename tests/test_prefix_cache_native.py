@@ -8,6 +8,7 @@ import hashlib
 import random
 
 import pytest
+import torch
 
 import oracle.prefix_cache as opc
 import paged_kv_cache_117_gb300 as pkv
@@ -116,3 +117,31 @@ def test_errors():
     assert pc.num_free() == 2 and pc.table(0) == ([], 0)   # refused whole
     with pytest.raises(pkv.PkvError):
         pc.free_sequence(7)
+
+
+@pytest.mark.parametrize("bad", [
+    torch.tensor([1, 2, 2**31], dtype=torch.int64),     # would wrap to a negative id
+    torch.tensor([1.0, 2.0]),                             # not integers
+    torch.tensor([True, False]),
+    [1, 2**31],
+])
+def test_token_ids_that_do_not_fit_int32_are_refused(bad):
+    """Token ids reach the C calls as int32: a value that does not fit (or a
+    tensor that is not integral) is refused before the call, whether it comes
+    as a tensor or a list, instead of being wrapped into another id."""
+    pc = pkv.PrefixCache(8, 4)
+    with pytest.raises(ValueError):
+        pc.add_sequence(0, bad)
+    with pytest.raises(ValueError):
+        pkv.chain_keys(bad, 1)
+    assert pc.num_free() == 8
+
+
+def test_sequence_ids_that_do_not_fit_int64_are_refused():
+    bm = pkv.BlockManager(8, 4)
+    bm.add_sequence(0)
+    with pytest.raises(ValueError):
+        bm.append(torch.tensor([0.0]))
+    with pytest.raises(ValueError):
+        bm.append([2**63])
+    assert bm.num_free() == 8

@@ -4,9 +4,11 @@ paged_attention_decode_noalloc serves callers that cannot allocate device
 memory for a workspace (a memory manager that owns all device memory, a
 plugin with a fixed budget, a loop that must not call cudaMalloc); it uses a
 scratch array inside the library instead.  This file calls it through the C
-ABI twice in a row, with different queries, and checks each result against
-paged_attention_decode with a caller-allocated workspace on the same inputs,
-at the tolerance the parity tests use.  It is collected last so that a run
+ABI several times in a row, with different queries and partition sizes, and
+requires each result to equal, bit for bit, paged_attention_decode with a
+caller-allocated workspace on the same inputs (the same kernel runs; only the
+scratch differs), and to lie within the parity tests' tolerance of the fp64
+oracle.  It is collected last so that a run
 stopping at the first failure has already run every other test; it also runs
 on its own in a fresh process.
 """
@@ -31,20 +33,27 @@ def pkv():
 
 
 def test_noalloc_matches_workspace_entry_point_twice(pkv):
+    import oracle.paged_ops as ops
     w = wl.scaled(wl.LLAMA8B, 12, num_blocks=1500)
-    pt = 64                                   # several partitions per sequence
     plan = gh.plan_step(w)
     k, v = wl.make_pool(w, "cuda")
     q, key, value = wl.make_step_inputs(w, "cuda")
+    q2 = torch.randn(q.shape, generator=torch.Generator().manual_seed(5)).to(q.dtype).cuda()
     tables = gh.table_tensor(plan).cuda()
     lens = torch.tensor(plan.lens, dtype=torch.int32, device="cuda")
-    assert max(-(-L // pt) for L in plan.lens) > 1
-    need = pkv.paged_attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
-                                               tables.shape[1] * w.block_size, pt)
-    assert 0 < need <= pkv.NOALLOC_SCRATCH_BYTES
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    for call in range(2):
-        qc = q if call == 0 else torch.randn_like(q, dtype=torch.float32).to(q.dtype)
+    # several partitions per sequence; the later calls change the partition
+    # size both ways, so a call finds the array holding counters and records
+    # of a call with more (then fewer) partitions than its own
+    calls = [(q, 64), (q2, 64), (q, 128), (q2, 16)]
+    assert max(-(-L // 64) for L in plan.lens) > 1
+    want = {}
+    for qi, qc in enumerate((q, q2)):
+        want[qi] = ops.attend(qc.cpu(), k.cpu(), v.cpu(), plan.tables, plan.lens, w.scale)
+    for call, (qc, pt) in enumerate(calls):
+        need = pkv.paged_attention_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                   tables.shape[1] * w.block_size, pt)
+        assert 0 < need <= pkv.NOALLOC_SCRATCH_BYTES
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         ref = torch.empty(q.shape, dtype=torch.float32, device="cuda")
         pkv.paged_attention_decode(ref, qc, k, v, tables, lens, w.scale, partition_tokens=pt,
                                    workspace=ws)
@@ -52,9 +61,11 @@ def test_noalloc_matches_workspace_entry_point_twice(pkv):
         pkv.paged_attention_decode_noalloc(got, qc, k, v, tables, lens, w.scale,
                                            partition_tokens=pt)
         torch.cuda.synchronize()
-        assert torch.isfinite(got).all()
-        err = (got - ref).abs().max().item()
-        assert err <= ATOL, f"call {call}: max abs diff {err:.3e}"
+        # the same kernel on the same inputs, only the scratch differs: the
+        # results must be identical bit for bit
+        assert torch.equal(got, ref), f"call {call}: differs from the workspace entry point"
+        err = (got.double().cpu() - want[0 if qc is q else 1]).abs().max().item()
+        assert err <= ATOL, f"call {call}: max abs error {err:.3e} against the fp64 oracle"
     assert pkv.read_device_flags(clear=True) == 0
 
 
