@@ -84,8 +84,11 @@ def parse_args():
     ap.add_argument("--workload", default="llama8b", choices=sorted(TABLE_WIDTH_TOKENS))
     ap.add_argument("--partition", type=int, default=None,
                     help="partition_tokens (default: the workload's, 512)")
-    ap.add_argument("--cpu-seqs", type=int, default=256,
-                    help="sequences in the CPU-oracle sample")
+    ap.add_argument("--cpu-workers", type=int, default=0,
+                    help="oracle worker processes for the CPU baseline (default: all cores)")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="default run: time only the headline workload, not the other "
+                         "decode configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step: one K/V pool per layer, shared block tables")
@@ -176,14 +179,21 @@ def build_metadata(w, manager="native"):
     return lens0, [list(t) for t in tables], width, slots
 
 
-def build_shared_step(w):
+def _manager(manager):
+    """The block-manager class: the library's (default) or the one given."""
+    if manager is not None:
+        return manager
+    import paged_kv_cache_117_gb300 as pkv
+    return pkv.BlockManager
+
+
+def build_shared_step(w, manager=None):
     """Parallel-sampling state built by the library's block manager: prompts,
     forks, each sample's own tokens (with the copies they caused), then this
     step's token of every sample.  Returns lens, tables, width, the step's
     slots and copy pairs, and the copies made while building the state."""
-    import paged_kv_cache_117_gb300 as pkv
     plan = wl.shared_prefix_plan(w)
-    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    bm = _manager(manager)(w.num_blocks, w.block_size, wl.free_block_order(w))
     S = plan.prompts * plan.samples
     setup = []
     for p in range(plan.prompts):
@@ -201,14 +211,13 @@ def build_shared_step(w):
     return list(lens), [list(t) for t in tables], width, slots, pairs, setup
 
 
-def build_beam_step(w):
+def build_beam_step(w, manager=None):
     """Beam-search state built by the library's block manager: prompts, beam
     forks, then every history step's forks, frees and one token per surviving
     beam.  Returns lens, tables, width, the measured step's slots and copy
     pairs, and the history as (pairs, slots) per step (to replay on a pool)."""
-    import paged_kv_cache_117_gb300 as pkv
     plan = wl.beam_plan(w)
-    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    bm = _manager(manager)(w.num_blocks, w.block_size, wl.free_block_order(w))
     R, W = plan.requests, plan.width
     for r in range(R):
         bm.add_sequence(r * W)
@@ -229,14 +238,13 @@ def build_beam_step(w):
     return list(lens), [list(t) for t in tables], width, slots, pairs, hist
 
 
-def build_chunked_step(w):
+def build_chunked_step(w, manager=None):
     """Chunked-prefill state built by the library's block manager: every
     sequence's earlier chunks, then this step's chunk.  Returns lens, tables,
     width, the chunk rows' slots, the per-sequence query counts and
     query_start."""
-    import paged_kv_cache_117_gb300 as pkv
     prior, counts = wl.chunk_plan(w)
-    bm = pkv.BlockManager(w.num_blocks, w.block_size, wl.free_block_order(w))
+    bm = _manager(manager)(w.num_blocks, w.block_size, wl.free_block_order(w))
     for s, c0 in enumerate(prior):
         bm.add_sequence(s)
         if c0:
@@ -250,15 +258,19 @@ def build_chunked_step(w):
     return list(lens), [list(t) for t in tables], width, slots, counts, qs
 
 
-def build_prefix_step(w):
+def build_prefix_step(w, manager=None):
     """Prefix-caching state built by the library's prefix-cache manager: one
     earlier request per system prompt prefilled it (its full blocks stay
     cached after it finished), then every request looks its prompt up and
     prefills only the rest.  Returns lens, tables, width, slots, counts,
     query_start and the prompt tokens the cache saved."""
-    import paged_kv_cache_117_gb300 as pkv
     plan = wl.prefix_plan(w)
-    pc = pkv.PrefixCache(w.num_blocks, w.block_size, wl.free_block_order(w))
+    if manager is None:
+        import paged_kv_cache_117_gb300 as pkv
+        cache_cls = pkv.PrefixCache
+    else:   # the reference arm: the oracle's prefix cache
+        from oracle.prefix_cache import PrefixCache as cache_cls
+    pc = cache_cls(w.num_blocks, w.block_size, wl.free_block_order(w))
     for i, sysp in enumerate(plan.systems):
         sid = len(plan.prompts) + i
         warm = sysp + [0]
@@ -268,7 +280,7 @@ def build_prefix_step(w):
     slots, counts, saved = [], [], 0
     for r, prompt in enumerate(plan.prompts):
         c = pc.add_sequence(r, prompt)
-        slots.append(pc.append(r, prompt[c:]))
+        slots.append(torch.as_tensor(pc.append(r, prompt[c:]), dtype=torch.int64))
         counts.append(len(prompt) - c)
         saved += c
     tables, lens = zip(*(pc.table(r) for r in range(len(plan.prompts))))
@@ -279,11 +291,11 @@ def build_prefix_step(w):
     return list(lens), [list(t) for t in tables], width, torch.cat(slots), counts, qs, saved
 
 
-def build_multiquery_step(w):
+def build_multiquery_step(w, manager=None):
     """(lens, tables, width, slots, counts, query_start, description) of a
     multi-query workload."""
     if w.lens_kind == "prefix":
-        lens, tables, width, slots, counts, qs, saved = build_prefix_step(w)
+        lens, tables, width, slots, counts, qs, saved = build_prefix_step(w, manager)
         n_sys, sys_len, q_len = w.lens_args
         desc = (f"{w.name}: {w.num_seqs} requests, each one of {n_sys} system prompts of "
                 f"{sys_len} tokens + its own {q_len}-token question (seeded token ids); the system "
@@ -294,7 +306,7 @@ def build_multiquery_step(w):
                 f"{str(w.dtype).replace('torch.', '')}, block {w.block_size}, {w.num_blocks}-block pool")
         return lens, tables, width, slots, counts, qs, desc
     prior, _ = wl.chunk_plan(w)
-    lens, tables, width, slots, counts, qs = build_chunked_step(w)
+    lens, tables, width, slots, counts, qs = build_chunked_step(w, manager)
     return lens, tables, width, slots, counts, qs, chunked_desc(w, width, prior, counts)
 
 
@@ -506,11 +518,6 @@ def max_over_ranks(world, x, device):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the only place bench.py touches oracle/)
 
-def sample_blocks(tables, nseq):
-    seqs = list(range(min(nseq, len(tables))))
-    return seqs, sorted({b for s in seqs for b in tables[s]})
-
-
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
@@ -523,26 +530,174 @@ def cpu_model():
     return platform.processor() or platform.machine()
 
 
-def oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value, slots, seqs):
-    """fp64 oracle over ``seqs``: KV write then attention, on a compact CPU
-    pool ``kc``/``vc`` holding the blocks ``ids``.  Returns (seconds,
-    algorithmic bytes of the sample, threads used)."""
+def _oracle_worker(conn):
+    """One oracle worker process.  It receives its share of a sample once
+    ("load"), then runs the fp64 oracle on it each time it is told to ("go"),
+    on a fresh copy of its compact pool, with one torch thread, and reports
+    its own busy seconds."""
+    import pickle
+    torch.set_num_threads(1)
     import oracle.paged_ops as ops
-    remap = {b: i for i, b in enumerate(ids)}
+    job = None
+    while True:
+        msg = pickle.loads(conn.recv_bytes())
+        if msg[0] == "stop":
+            break
+        if msg[0] == "load":
+            job = msg[1]
+            conn.send_bytes(pickle.dumps("ready"))
+            continue
+        kc, vc = job["k"].clone(), job["v"].clone()
+        t0 = time.perf_counter()
+        oracle_step(ops, job, kc, vc)
+        conn.send_bytes(pickle.dumps(("done", time.perf_counter() - t0)))
+
+
+def oracle_step(ops, job, kc, vc):
+    """The oracle's step on one job, in place on the pool copy kc/vc: the
+    copies, the write of the new rows, then attention.  Returns the output."""
+    ops.copy_blocks(kc, vc, job["pairs"])
+    ops.write_kv(kc, vc, job["key"], job["value"], job["slots"])
+    if job["kind"] == "decode":
+        return ops.attend(job["q"], kc, vc, job["tables"], job["lens"], job["scale"])
+    return ops.attend_chunked(job["q"], kc, vc, job["tables"], job["lens"], job["qs"],
+                              job["scale"])
+
+
+class OraclePool:
+    """Worker processes for timing the fp64 oracle across the host's cores.
+
+    Started with the spawn method (safe whatever CUDA state the parent is
+    in).  A sample is split by sequence into one job per worker; the jobs are
+    sent and loaded first, then all workers are started together and the
+    wall time from the start signal to the last worker's reply is the
+    sample's time.  Each worker runs torch with one thread, so the number of
+    workers that received a job is the number of cores used."""
+
+    def __init__(self, workers):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.workers = []
+        for _ in range(max(1, workers)):
+            parent, child = ctx.Pipe()
+            proc = ctx.Process(target=_oracle_worker, args=(child,), daemon=True)
+            proc.start()
+            child.close()
+            self.workers.append((proc, parent))
+        self.active = []
+
+    def __len__(self):
+        return len(self.workers)
+
+    def load(self, jobs):
+        import pickle
+        assert len(jobs) <= len(self.workers)
+        self.active = [c for (_, c), _ in zip(self.workers, jobs)]
+        for c, job in zip(self.active, jobs):
+            c.send_bytes(pickle.dumps(("load", job)))
+        for c in self.active:
+            assert pickle.loads(c.recv_bytes()) == "ready"
+
+    def run(self):
+        """(wall seconds, per-worker busy seconds) of one pass over the
+        loaded sample."""
+        import pickle
+        go = pickle.dumps(("go",))
+        t0 = time.perf_counter()
+        for c in self.active:
+            c.send_bytes(go)
+        busy = [pickle.loads(c.recv_bytes())[1] for c in self.active]
+        return time.perf_counter() - t0, busy
+
+    def close(self):
+        import pickle
+        for proc, c in self.workers:
+            try:
+                c.send_bytes(pickle.dumps(("stop",)))
+            except Exception:
+                pass
+        for proc, c in self.workers:
+            proc.join(timeout=10)
+            if proc.is_alive():
+                proc.kill()
+        self.workers = []
+
+
+def split_by_work(seqs, work, n):
+    """Sequences spread over at most n workers, longest first to the least
+    loaded (each part kept in sequence order)."""
+    parts, loads = [[] for _ in range(n)], [0] * n
+    for s in sorted(seqs, key=lambda s: -work[s]):
+        i = loads.index(min(loads))
+        parts[i].append(s)
+        loads[i] += work[s]
+    return [sorted(p) for p in parts if p]
+
+
+def oracle_jobs(w, kind, seqs_parts, tables, lens, pairs, fetch, q_rows, key_rows, value_rows,
+                slots, row_start=None):
+    """One oracle job per part: a compact pool holding the part's blocks (and
+    the sources of the step's copies into them), its copy pairs, new rows and
+    slots, queries, tables and lengths, all renumbered into that pool.
+    ``fetch(ids)`` returns the pool blocks ``ids`` as CPU tensors.  Decode:
+    row s of q/key/value/slots belongs to sequence s.  Chunked: sequence s
+    owns rows row_start[s] .. row_start[s+1]-1."""
     B = w.block_size
-    loc_slots = [remap[slots[s] // B] * B + slots[s] % B for s in seqs]
-    tabs = [[remap[b] for b in tables[s]] for s in seqs]
-    qc, kk, vv = q[seqs].cpu(), key[seqs].cpu(), value[seqs].cpu()
-    kc, vc = kc.clone(), vc.clone()
-    t0 = time.perf_counter()
-    ops.write_kv(kc, vc, kk, vv, loc_slots)
-    ops.attend(qc, kc, vc, tabs, [lens[s] for s in seqs], w.scale)
-    dt = time.perf_counter() - t0
-    nbytes = algorithmic_bytes(w, [lens[s] for s in seqs], width, 0, w.elem_bytes)
-    return dt, nbytes["kv"] + nbytes["write"], torch.get_num_threads()
+    jobs = []
+    for part in seqs_parts:
+        ids = {b for s in part for b in tables[s]}
+        step_pairs = [(int(a), int(b)) for a, b in pairs if int(b) in ids]
+        ids |= {a for a, _ in step_pairs}
+        ids = sorted(ids)
+        remap = {b: i for i, b in enumerate(ids)}
+        kc, vc = fetch(ids)
+        rows = ([s for s in part] if row_start is None else
+                [r for s in part for r in range(row_start[s], row_start[s + 1])])
+        loc = [remap[int(slots[r]) // B] * B + int(slots[r]) % B for r in rows]
+        job = {"kind": kind, "k": kc, "v": vc, "scale": w.scale,
+               "pairs": [(remap[a], remap[b]) for a, b in step_pairs],
+               "key": key_rows[rows].cpu(), "value": value_rows[rows].cpu(), "slots": loc,
+               "q": q_rows[rows].cpu(), "tables": [[remap[b] for b in tables[s]] for s in part],
+               "lens": [lens[s] for s in part]}
+        if row_start is not None:
+            qs = [0]
+            for s in part:
+                qs.append(qs[-1] + row_start[s + 1] - row_start[s])
+            job["qs"] = qs
+        jobs.append(job)
+    return jobs
 
 
-# ---------------------------------------------------------------------------
+def device_fetch(k, v):
+    def fetch(ids):
+        idx = torch.tensor(ids, dtype=torch.int64, device=k.device)
+        return k[idx].cpu(), v[idx].cpu()
+    return fetch
+
+
+def cpu_baseline_decode(pool, w, lens, tables, width, pairs, fetch, q, key, value, slots):
+    """The fp64 oracle's step (copies, KV write, attention) over the whole
+    batch, split by sequence over the pool's workers."""
+    S = len(lens)
+    parts = split_by_work(range(S), lens, len(pool))
+    pairs = [tuple(p) for p in (pairs.tolist() if torch.is_tensor(pairs) else pairs)]
+    pool.load(oracle_jobs(w, "decode", parts, tables, lens, pairs, fetch, q, key, value,
+                          slots.tolist() if torch.is_tensor(slots) else slots))
+    wall, busy = pool.run()
+    b = algorithmic_bytes(w, lens, width, 0, w.elem_bytes, len(pairs))["step"]
+    return {"value": b / wall / 1e9, "unit": UNIT, "cores": len(parts), "kind": "oracle",
+            "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
+            "sample": f"fp64 oracle (torch CPU ops) step of all {S} sequences: "
+                      f"{len(pairs)} block copies, KV write, attention; split by sequence over "
+                      f"{len(parts)} worker processes with one torch thread each, {wall:.2f} s "
+                      f"wall ({sum(busy):.1f} s busy); bytes = the step's algorithmic bytes "
+                      f"without split-context records"}
+
+
+# Decode configurations measured after the headline one in a default run
+# (each under "other_configs" of the one JSON line).
+OTHER_DECODE_CONFIGS = ("opt13b", "qwen72b", "shared")
+
 
 def run_native(a, world, rank, local):
     import paged_kv_cache_117_gb300 as pkv
@@ -552,9 +707,84 @@ def run_native(a, world, rank, local):
     barrier(world)
     pkv.load()
     assert torch.cuda.is_available(), "the native benchmark needs a GPU"
+    w = select_workload(a)
+    others = []
+    if (not a.no_other_configs and w is wl.LLAMA8B and a.layers == 1 and not a.graph
+            and a.partition is None):
+        others = [wl.WORKLOADS[n] for n in OTHER_DECODE_CONFIGS]
+    pool = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        pool = OraclePool(a.cpu_workers or os.cpu_count() or 1)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = select_workload(a)
+    try:
+        res = measure_decode(a, w, world, rank, dev, pool)
+        if others:
+            sub = argparse.Namespace(**{**vars(a), "partition": None, "layers": 1,
+                                        "graph": False})
+            res["other_configs"] = []
+            for wo in others:
+                r = measure_decode(sub, wo, world, rank, dev, pool)
+                for key_ in ("metric", "unit", "n_gpus", "steps", "warmup", "higher_is_better",
+                             "scaling", "vs_baseline", "data"):
+                    r.pop(key_, None)
+                res["other_configs"].append(r)
+        if others:
+            res["block_copy"] = measure_block_copy(wl.LLAMA8B, dev, a.steps, a.warmup)
+    finally:
+        if pool is not None:
+            pool.close()
+    return res
+
+
+def measure_block_copy(w, dev, steps, warmup, sizes=(16, 256, 4096)):
+    """paged_block_copy alone on a pool of the workload's shape: P disjoint
+    (src, dst) pairs drawn from a seeded permutation, for each P with the scan
+    check (no workspace) and with the counter workspace.  GB/s counts every
+    copied block read once and written once in both pools."""
+    import paged_kv_cache_117_gb300 as pkv
+    k, v = wl.make_pool_chunked(w, dev)
+    ws = pkv.block_copy_workspace(k)
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(w.seed + 6000))
+    block_bytes = w.block_size * w.num_kv_heads * w.head_dim * w.elem_bytes
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, kind = peak_hbm()
+    rows = []
+    for P in sizes:
+        pairs = torch.stack([perm[:P], perm[P:2 * P]], 1).to(dev)
+        for wsp in (None, ws):
+            for _ in range(max(3, warmup)):
+                flush()
+                pkv.paged_block_copy(k, v, pairs, workspace=wsp)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+            torch.cuda.synchronize()
+            host_head_start()
+            for e0, e1 in evs:
+                flush()
+                e0.record(stream)
+                pkv.paged_block_copy(k, v, pairs, workspace=wsp)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+            nbytes = P * block_bytes * 2 * 2 + P * 16
+            gbs = nbytes / (us * 1e-6) / 1e9
+            rows.append({"pairs": P, "check": "scan" if wsp is None else "counters",
+                         "us": round(us, 2), "gbs": round(gbs, 1),
+                         "frac": round(gbs / peak, 4), "launches": 1 if wsp is None else 3})
+    assert pkv.read_device_flags(clear=True) == 0
+    return {"workload": f"{w.name}-shaped pool ({w.num_blocks} blocks of {block_bytes} B per "
+                        f"pool), disjoint pairs from a seeded permutation; L2 flushed before "
+                        f"each call; bytes = each copied block read and written in K and V",
+            "peak": peak, "peak_kind": f"{kind} hbm_gbs", "rows": rows}
+
+
+def measure_decode(a, w, world, rank, dev, pool):
+    """One decode workload: build its state, time the step and the attention
+    call, the end-to-end step through host buffers, and (with a pool) the
+    fp64 oracle's step on the host cores.  Returns the bench line's fields."""
+    import paged_kv_cache_117_gb300 as pkv
     pt = w.partition_tokens if a.partition is None else a.partition
     k, v = wl.make_pool_chunked(w, dev)
     hist = None
@@ -573,7 +803,6 @@ def run_native(a, world, rank, local):
     q, key, value = wl.make_step_inputs(w, dev)
     tab, lens_t, slots = tab_cpu.to(dev), lens_cpu.to(dev), slots_cpu.to(dev)
     pairs = pairs_cpu.to(dev)
-    import dataclasses
     layers = [(k, v, q, key, value)]
     for li in range(1, a.layers):   # one pool per layer; one block id = one slot range in all
         wl_l = dataclasses.replace(w, seed=w.seed + 10 * li)
@@ -599,18 +828,12 @@ def run_native(a, world, rank, local):
     fused = a.kv_write == "append"
     launches_per_step = a.layers * ((1 if pairs.shape[0] else 0) + (0 if fused else 1) + 2)
 
-    # CPU-oracle sample: inputs snapshot before any library kernel runs
+    # CPU-oracle step over the whole batch: the pool's blocks are fetched
+    # before any kernel of the step runs on them
     cpu = None
-    if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        seqs, ids = sample_blocks(tables, a.cpu_seqs)
-        idx = torch.tensor(ids, device=dev)
-        dt, b, threads = oracle_sample_time(w, lens, tables, width, k[idx].cpu(), v[idx].cpu(),
-                                            ids, q, key, value, slots_cpu.tolist(), seqs)
-        cpu = {"value": b / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
-               "sample": f"fp64 oracle (torch CPU ops) KV write + attention of the first "
-                         f"{min(a.cpu_seqs, w.num_seqs)} of {w.num_seqs} sequences, "
-                         f"{dt:.1f} s; bytes = unique K/V rows read + new rows written"}
+    if pool is not None:
+        cpu = cpu_baseline_decode(pool, w, lens, tables, width, pairs_cpu, device_fetch(k, v),
+                                  q, key, value, slots_cpu)
 
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -791,21 +1014,24 @@ def chunked_desc(w, width, prior, counts):
             f"causal within each chunk, q/K/V ~ N(0,1)")
 
 
-def oracle_chunk_sample(w, lens, tables, counts, qs, kc, vc, ids, q, key, value, slots, seq):
-    """fp64 oracle: one sequence's chunk written and attended, on a compact CPU
-    pool holding the blocks ``ids``.  Returns (seconds, FLOPs, threads)."""
-    import oracle.paged_ops as ops
-    remap = {b: i for i, b in enumerate(ids)}
-    B = w.block_size
-    r0, r1 = qs[seq], qs[seq + 1]
-    loc = [remap[int(x) // B] * B + int(x) % B for x in slots[r0:r1]]
-    kc, vc = kc.clone(), vc.clone()
-    t0 = time.perf_counter()
-    ops.write_kv(kc, vc, key[r0:r1], value[r0:r1], loc)
-    ops.attend_chunked(q[r0:r1], kc, vc, [[remap[b] for b in tables[seq]]], [lens[seq]],
-                       [0, r1 - r0], w.scale)
-    dt = time.perf_counter() - t0
-    return dt, chunked_flops(w, [lens[seq]], [counts[seq]]), torch.get_num_threads()
+def cpu_baseline_chunked(pool, w, lens, tables, counts, qs, fetch, q, key, value, slots,
+                         seqs=None):
+    """The fp64 oracle's chunked step (write of the chunk rows, multi-query
+    attention) over ``seqs`` (default: the whole batch), split by sequence
+    over the pool's workers."""
+    seqs = list(range(len(lens))) if seqs is None else list(seqs)
+    work = {s: counts[s] * lens[s] for s in seqs}
+    parts = split_by_work(seqs, work, len(pool))
+    pool.load(oracle_jobs(w, "chunked", parts, tables, lens, [], fetch, q, key, value,
+                          slots.tolist() if torch.is_tensor(slots) else slots, row_start=qs))
+    wall, busy = pool.run()
+    fl = chunked_flops(w, [lens[s] for s in seqs], [counts[s] for s in seqs])
+    return {"value": fl / wall / 1e12, "unit": "TFLOP/s", "cores": len(parts), "kind": "oracle",
+            "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
+            "sample": f"fp64 oracle (torch CPU ops) write + chunked attention of {len(seqs)} of "
+                      f"{len(lens)} sequences ({sum(counts[s] for s in seqs)} query rows), split "
+                      f"by sequence over {len(parts)} worker processes with one torch thread "
+                      f"each, {wall:.2f} s wall ({sum(busy):.1f} s busy)"}
 
 
 def run_native_chunked(a, world, rank, local):
@@ -837,15 +1063,12 @@ def run_native_chunked(a, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        ids = sorted(set(tables[0]))
-        idx = torch.tensor(ids, device=dev)
-        dt, fl, threads = oracle_chunk_sample(w, lens, tables, counts, qs, k[idx].cpu(),
-                                              v[idx].cpu(), ids, q.cpu(), key.cpu(),
-                                              value.cpu(), slots_cpu.tolist(), 0)
-        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "cpu": f"{cpu_model()}, {os.cpu_count()} logical cores",
-               "sample": f"fp64 oracle (torch CPU ops) write + chunked attention of sequence 0 "
-                         f"({counts[0]} queries over {lens[0]} tokens), {dt:.1f} s"}
+        pool = OraclePool(min(len(lens), a.cpu_workers or os.cpu_count() or 1))
+        try:
+            cpu = cpu_baseline_chunked(pool, w, lens, tables, counts, qs, device_fetch(k, v),
+                                       q, key, value, slots_cpu)
+        finally:
+            pool.close()
 
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -1012,84 +1235,172 @@ def prefix_manager_cost(w, rounds=20):
                     "blocks cached); us_per_request is the miss cost"}
 
 
+class OracleManager:
+    """The oracle's block manager behind the library manager's calls
+    (append of several sequences, tables as lists), for the reference arm,
+    which runs no library code."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        from oracle.block_manager import BlockManager
+        self.bm = BlockManager(num_blocks, block_size, free_order)
+
+    def add_sequence(self, seq):
+        self.bm.add_sequence(seq)
+
+    def fork(self, parent, child):
+        self.bm.fork(parent, child)
+
+    def free_sequence(self, seq):
+        self.bm.free_sequence(seq)
+
+    def append(self, seqs):
+        slots, pairs = [], []
+        for s in seqs:
+            slot, cow = self.bm.append(int(s))
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(list(cow))
+        return (torch.tensor(slots, dtype=torch.int64),
+                torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2))
+
+    def append_tokens(self, seq, count):
+        return self.append([seq] * int(count))
+
+    def table(self, seq):
+        return list(self.bm.tables[seq]), self.bm.lens[seq]
+
+
+def host_pool_fetch(w, ids, seed):
+    """K/V values for the pool blocks ``ids`` only, N(0,1) on the host (the
+    reference arm touches no GPU); returns a fetch(ids) over them."""
+    g = torch.Generator().manual_seed(seed)
+    shape = (len(ids), w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.randn(shape, generator=g).to(w.dtype)
+    vc = torch.randn(shape, generator=g).to(w.dtype)
+    pos = {b: i for i, b in enumerate(ids)}
+
+    def fetch(sub):
+        idx = torch.tensor([pos[b] for b in sub], dtype=torch.int64)
+        return kc[idx], vc[idx]
+    return fetch
+
+
+def reference_line(metric, unit, val, ms, a, world, desc, cores, sample, digits):
+    return {"impl": "reference", "metric": metric, "value": round(val, digits), "unit": unit,
+            "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc},
+            "cpu_baseline": {"value": round(val, digits), "unit": unit, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, digits), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def run_reference(a, world, rank, local):
-    """The fp64 CPU oracle as it stands, one bounded sample per step."""
+    """The fp64 CPU oracle as it stands: each step is the oracle's decode step
+    (copies, KV write, attention) of the whole batch, split by sequence over
+    worker processes on the host's cores."""
     if rank != 0:
         return None
     w = select_workload(a)
     if w.lens_kind == "shared":
-        lens, tables, width, slot_t, _, _ = build_shared_step(w)
+        lens, tables, width, slots, pairs, _ = build_shared_step(w, OracleManager)
     elif w.lens_kind == "beam":
-        lens, tables, width, slot_t, _, _ = build_beam_step(w)
+        lens, tables, width, slots, pairs, _ = build_beam_step(w, OracleManager)
     else:
-        lens, tables, width, slot_t = build_metadata(w, manager="oracle")
-    # inputs with the same distributions, generated on the CPU for just the
-    # blocks the sample reads (no GPU needed)
-    nseq = max(1, min(w.num_seqs, 4))
-    seqs, ids = sample_blocks(tables, nseq)
-    g = torch.Generator().manual_seed(w.seed + 2000)
-    shape = (len(ids), w.block_size, w.num_kv_heads, w.head_dim)
-    kc = torch.randn(shape, generator=g).to(w.dtype)
-    vc = torch.randn(shape, generator=g).to(w.dtype)
+        lens, tables, width, slots = build_metadata(w, manager="oracle")
+        pairs = torch.zeros((0, 2), dtype=torch.int64)
+    pairs = [tuple(p) for p in pairs.tolist()]
+    ids = sorted({b for t in tables for b in t} | {p[0] for p in pairs})
+    fetch = host_pool_fetch(w, ids, w.seed + 2000)
     q, key, value = wl.make_step_inputs(w, "cpu")
-    slots = slot_t.tolist()
-    times, nbytes, threads = [], 0, torch.get_num_threads()
-    for i in range(max(3, a.warmup) + a.steps):
-        dt, b, threads = oracle_sample_time(w, lens, tables, width, kc, vc, ids, q, key, value,
-                                            slots, seqs)
-        if i >= max(3, a.warmup):
-            times.append(dt)
-            nbytes = b
+    pool = OraclePool(a.cpu_workers or os.cpu_count() or 1)
+    try:
+        parts = split_by_work(range(len(lens)), lens, len(pool))
+        pool.load(oracle_jobs(w, "decode", parts, tables, lens, pairs, fetch, q, key, value,
+                              slots.tolist()))
+        times = []
+        for i in range(max(3, a.warmup) + a.steps):
+            wall, _ = pool.run()
+            if i >= max(3, a.warmup):
+                times.append(wall)
+    finally:
+        pool.close()
+    nbytes = algorithmic_bytes(w, lens, width, 0, w.elem_bytes, len(pairs))["step"]
     ms = 1e3 * sum(times) / len(times)
     val = nbytes / (ms * 1e-3) / 1e9
-    sample = (f"fp64 oracle KV write + attention of the first {nseq} of {w.num_seqs} sequences "
-              f"per step ({nbytes / 1e6:.1f} MB algorithmic)")
-    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": UNIT,
-            "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
-            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w, width)},
-            "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": threads,
-                             "kind": "oracle", "sample": sample},
-            "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+    sample = (f"fp64 oracle step of all {len(lens)} sequences ({len(pairs)} block copies, KV "
+              f"write, attention; {nbytes / 1e6:.1f} MB algorithmic) per step, split by sequence "
+              f"over {len(parts)} worker processes with one torch thread each")
+    return reference_line(METRIC, UNIT, val, ms, a, world, workload_desc(w, width), len(parts),
+                          sample, 4)
+
+
+def subchunk_jobs(w, seq, lens, tables, counts, qs, fetch, q, key, value, slots, n):
+    """One sequence's chunk split by query rows into about n jobs of equal
+    work: rows a..b-1 of a chunk of c rows in a sequence of L tokens are the
+    last b - a rows of a sequence of L - c + b tokens, so each job is the
+    oracle's chunked call on that shorter sequence (its write covers rows
+    0..b-1 of the chunk, which those queries see)."""
+    L, c, r0 = lens[seq], counts[seq], qs[seq]
+    first = L - c                      # position of chunk row 0
+    total = sum(first + i + 1 for i in range(c))
+    bounds, acc, a0 = [], 0, 0
+    for i in range(c):
+        acc += first + i + 1
+        if acc >= total * (len(bounds) + 1) / n or i == c - 1:
+            bounds.append((a0, i + 1))
+            a0 = i + 1
+    ids = sorted(set(tables[seq]))
+    remap = {b: i for i, b in enumerate(ids)}
+    kc, vc = fetch(ids)
+    B = w.block_size
+    jobs = []
+    for a_, b_ in bounds:
+        rows = list(range(r0, r0 + b_))
+        jobs.append({"kind": "chunked", "k": kc, "v": vc, "scale": w.scale, "pairs": [],
+                     "key": key[rows].cpu(), "value": value[rows].cpu(),
+                     "slots": [remap[int(slots[r]) // B] * B + int(slots[r]) % B for r in rows],
+                     "q": q[r0 + a_:r0 + b_].cpu(), "tables": [[remap[x] for x in tables[seq]]],
+                     "lens": [first + b_], "qs": [0, b_ - a_]})
+    return jobs
 
 
 def run_reference_chunked(a, world, rank, local):
-    """The fp64 CPU oracle on the chunked workload: one sequence's chunk per
-    step (the shortest one, to bound the time)."""
+    """The fp64 CPU oracle on a chunked workload: each step is the shortest
+    sequence's chunk (write + multi-query attention), split by query rows
+    over worker processes on the host's cores (the whole batch would take
+    the oracle tens of seconds per step)."""
     if rank != 0:
         return None
     w = wl.WORKLOADS[a.workload]
-    lens, tables, width, slots, counts, qs, desc = build_multiquery_step(w)
+    lens, tables, width, slots, counts, qs, desc = build_multiquery_step(w, OracleManager)
     seq = min(range(len(lens)), key=lambda s: lens[s])
-    ids = sorted(set(tables[seq]))
-    g = torch.Generator().manual_seed(w.seed + 2000)
-    shape = (len(ids), w.block_size, w.num_kv_heads, w.head_dim)
-    kc = torch.randn(shape, generator=g).to(w.dtype)
-    vc = torch.randn(shape, generator=g).to(w.dtype)
+    fetch = host_pool_fetch(w, sorted(set(tables[seq])), w.seed + 2000)
     T = qs[-1]
+    g = torch.Generator().manual_seed(w.seed + 3000)
     q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g).to(w.dtype)
     key, value = wl.make_rows(w, 0, T)
-    times, fl, threads = [], 0, torch.get_num_threads()
-    for i in range(max(3, a.warmup) + a.steps):
-        dt, fl, threads = oracle_chunk_sample(w, lens, tables, counts, qs, kc, vc, ids, q, key,
-                                              value, slots.tolist(), seq)
-        if i >= max(3, a.warmup):
-            times.append(dt)
+    pool = OraclePool(a.cpu_workers or os.cpu_count() or 1)
+    try:
+        jobs = subchunk_jobs(w, seq, lens, tables, counts, qs, fetch, q, key, value,
+                             slots.tolist(), len(pool))
+        pool.load(jobs)
+        times = []
+        for i in range(max(3, a.warmup) + a.steps):
+            wall, _ = pool.run()
+            if i >= max(3, a.warmup):
+                times.append(wall)
+    finally:
+        pool.close()
+    fl = chunked_flops(w, [lens[seq]], [counts[seq]])
     ms = 1e3 * sum(times) / len(times)
     val = fl / (ms * 1e-3) / 1e12
     sample = (f"fp64 oracle write + chunked attention of sequence {seq} per step "
-              f"({counts[seq]} queries over {lens[seq]} tokens)")
-    return {"impl": "reference", "metric": CHUNK_METRIC, "value": round(val, 6),
-            "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": max(3, a.warmup),
-            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": desc},
-            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": threads,
-                             "kind": "oracle", "sample": sample},
-            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+              f"({counts[seq]} queries over {lens[seq]} tokens), split by query rows over "
+              f"{len(jobs)} worker processes with one torch thread each")
+    return reference_line(CHUNK_METRIC, "TFLOP/s", val, ms, a, world, desc, len(jobs), sample, 6)
 
 
 def main():

@@ -124,11 +124,45 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache,
  * skipped and flagged (PKV_FLAG_PAIR_CONFLICT) -- the copies of one call run
  * in no particular order -- and a pair naming a block outside [0, num_blocks)
  * is skipped and flagged (PKV_FLAG_PAIR_RANGE).  num_pairs == 0 is a no-op.
+ *
+ * Cost of the check: each CTA compares its pair with every other pair
+ * (O(num_pairs) reads per CTA, from L2), which is nothing for the few copies
+ * of a decode step.  For long pair lists (beam search forking many beams,
+ * a scheduler moving many requests at once) use paged_block_copy_ws, whose
+ * check costs O(1) per CTA.
  */
 pkv_status paged_block_copy(void *k_cache, void *v_cache,
                             const int64_t *block_pairs, int num_pairs,
                             int num_blocks, int block_size, int num_kv_heads,
                             int head_dim, pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * paged_block_copy_ws -- paged_block_copy with the pair check done through a
+ * caller-owned counter workspace, so that its cost does not grow with the
+ * number of pairs.  Same copies, same skips and flags, same results.
+ *
+ *   workspace        DEVICE memory of at least
+ *                    paged_block_copy_workspace_bytes(num_blocks) bytes
+ *                    (two uint32 counters per pool block), 256-byte aligned.
+ *                    It must be all zero before the first call; every call
+ *                    leaves it all zero again when its work on the stream is
+ *                    done, so allocate it zeroed once and reuse it.  Calls
+ *                    that share one workspace must not overlap in time
+ *                    (issue them on one stream).
+ *
+ * Three kernels run in stream order: a counting pass (per pair, one atomic
+ * increment of cnt_dst[dst] and of cnt_src[src]), the copy (a pair is
+ * skipped and flagged when cnt_dst[dst] > 1, or when cnt_src[dst] counts a
+ * src other than the pair's own), and a reset pass that zeroes the counters
+ * the counting pass raised.  A null workspace returns PKV_ERR_WORKSPACE;
+ * other errors as paged_block_copy.
+ */
+size_t paged_block_copy_workspace_bytes(int num_blocks);
+pkv_status paged_block_copy_ws(void *k_cache, void *v_cache,
+                               const int64_t *block_pairs, int num_pairs,
+                               int num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, pkv_dtype dtype, void *workspace,
+                               size_t workspace_bytes, pkv_stream_t stream);
 
 /*
  * paged_attention_decode -- single-query attention over the paged context.

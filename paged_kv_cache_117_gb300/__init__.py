@@ -10,4 +10,5 @@ from .binding import (  # noqa: F401
     paged_attention_decode, paged_attention_decode_noalloc, paged_attention_decode_append,
     paged_attention_chunked,
     paged_attention_workspace_bytes, paged_block_copy, paged_kv_write, read_device_flags,
+    block_copy_workspace, paged_block_copy_workspace_bytes,
 )

@@ -30,6 +30,8 @@ FLAG_PAIR_CONFLICT = 0x40
 EXPORTED_SYMBOLS = (
     "paged_kv_write",
     "paged_block_copy",
+    "paged_block_copy_ws",
+    "paged_block_copy_workspace_bytes",
     "paged_attention_decode",
     "paged_attention_workspace_bytes",
     "pkv_status_string",
@@ -78,6 +80,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.paged_kv_write.restype = ci
     lib.paged_block_copy.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp]
     lib.paged_block_copy.restype = ci
+    lib.paged_block_copy_ws.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, cs, vp]
+    lib.paged_block_copy_ws.restype = ci
+    lib.paged_block_copy_workspace_bytes.argtypes = [ci]
+    lib.paged_block_copy_workspace_bytes.restype = cs
     lib.paged_attention_decode.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, ci, ci, ci,
                                            ci, ci, ci, cf, ci, vp, cs, vp]
     lib.paged_attention_decode.restype = ci
@@ -193,16 +199,43 @@ def paged_kv_write(key, value, k_cache, v_cache, slot_mapping, stream=None) -> N
     _check("paged_kv_write", st)
 
 
-def paged_block_copy(k_cache, v_cache, block_pairs, stream=None) -> None:
-    """Copy whole blocks src -> dst for every row (src, dst) of int64 [P, 2]."""
+def paged_block_copy_workspace_bytes(num_blocks: int) -> int:
+    n = load().paged_block_copy_workspace_bytes(int(num_blocks))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid block copy workspace query")
+    return int(n)
+
+
+def block_copy_workspace(k_cache) -> torch.Tensor:
+    """A zeroed counter workspace for paged_block_copy(..., workspace=) on
+    k_cache's pool: allocate once, reuse for every call on that pool (each
+    call leaves it zeroed)."""
+    n = paged_block_copy_workspace_bytes(int(k_cache.shape[0]))
+    return torch.zeros(n, dtype=torch.uint8, device=k_cache.device)
+
+
+def paged_block_copy(k_cache, v_cache, block_pairs, workspace=None, stream=None) -> None:
+    """Copy whole blocks src -> dst for every row (src, dst) of int64 [P, 2].
+    With ``workspace`` (from block_copy_workspace) the pair check costs O(1)
+    per CTA (paged_block_copy_ws); without, each CTA scans the pair list
+    (paged_block_copy), which suits the few pairs of a decode step."""
     _need_cuda("paged_block_copy", k_cache, v_cache, block_pairs)
     N, B, H, D = _cache_dims(k_cache)
     if block_pairs.dtype != torch.int64:
         raise ValueError("block_pairs must be int64")
     P = int(block_pairs.shape[0]) if block_pairs.numel() else 0
-    st = load().paged_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, N, B,
-                                 H, D, _DTYPE_CODE.get(k_cache.dtype, -1), _stream(stream))
-    _check("paged_block_copy", st)
+    code = _DTYPE_CODE.get(k_cache.dtype, -1)
+    if workspace is None:
+        st = load().paged_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, N, B,
+                                     H, D, code, _stream(stream))
+        _check("paged_block_copy", st)
+        return
+    _need_cuda("paged_block_copy", workspace)
+    st = load().paged_block_copy_ws(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, N, B,
+                                    H, D, code, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check("paged_block_copy_ws", st)
 
 
 def paged_attention_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,

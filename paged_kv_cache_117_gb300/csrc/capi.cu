@@ -187,9 +187,13 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache, voi
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_kv_write launch");
 }
 
-pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_pairs,
-                            int num_pairs, int num_blocks, int block_size, int num_kv_heads,
-                            int head_dim, pkv_dtype dtype, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+pkv_status block_copy_impl(void *k_cache, void *v_cache, const int64_t *block_pairs,
+                           int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                           int head_dim, pkv_dtype dtype, void *workspace,
+                           size_t workspace_bytes, pkv_stream_t stream, const char *what) {
   if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_RANGE;
   if (!supported_cache_dtype(dtype)) return PKV_ERR_DTYPE;
   if (!supported_head_dim(head_dim) || !supported_block(block_size)) return PKV_ERR_SHAPE;
@@ -199,16 +203,50 @@ pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_p
     return PKV_ERR_ALIGN;
   const size_t block_bytes = (size_t)block_size * num_kv_heads * head_dim * 2;
   const size_t pool = block_bytes * num_blocks;
-  if (overlap(k_cache, pool, v_cache, pool) ||
-      overlap(block_pairs, (size_t)num_pairs * 16, k_cache, pool) ||
-      overlap(block_pairs, (size_t)num_pairs * 16, v_cache, pool))
+  const size_t pairs_sz = (size_t)num_pairs * 16;
+  if (overlap(k_cache, pool, v_cache, pool) || overlap(block_pairs, pairs_sz, k_cache, pool) ||
+      overlap(block_pairs, pairs_sz, v_cache, pool))
     return PKV_ERR_ALIAS;
+  if (workspace != nullptr) {
+    if (workspace_bytes < paged_block_copy_workspace_bytes(num_blocks)) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+    const size_t ws = (size_t)num_blocks * 8;
+    if (overlap(workspace, ws, k_cache, pool) || overlap(workspace, ws, v_cache, pool) ||
+        overlap(workspace, ws, block_pairs, pairs_sz))
+      return PKV_ERR_ALIAS;
+  }
   unsigned *flags = device_flags();
   if (!flags) return cuda_fail_msg("device flag word unavailable");
-  const cudaError_t e =
-      pkv::launch_block_copy(k_cache, v_cache, block_pairs, num_pairs, (long long)block_bytes,
-                             num_blocks, flags, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_block_copy launch");
+  const cudaError_t e = pkv::launch_block_copy(
+      k_cache, v_cache, block_pairs, num_pairs, (long long)block_bytes, num_blocks,
+      static_cast<unsigned *>(workspace), flags, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, what);
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_block_copy(void *k_cache, void *v_cache, const int64_t *block_pairs,
+                            int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                            int head_dim, pkv_dtype dtype, pkv_stream_t stream) {
+  return block_copy_impl(k_cache, v_cache, block_pairs, num_pairs, num_blocks, block_size,
+                         num_kv_heads, head_dim, dtype, nullptr, 0, stream,
+                         "paged_block_copy launch");
+}
+
+size_t paged_block_copy_workspace_bytes(int num_blocks) {
+  if (num_blocks <= 0) return (size_t)-1;
+  return pkv::round256((size_t)num_blocks * 8);
+}
+
+pkv_status paged_block_copy_ws(void *k_cache, void *v_cache, const int64_t *block_pairs,
+                               int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, pkv_dtype dtype, void *workspace,
+                               size_t workspace_bytes, pkv_stream_t stream) {
+  if (!workspace) return PKV_ERR_WORKSPACE;
+  return block_copy_impl(k_cache, v_cache, block_pairs, num_pairs, num_blocks, block_size,
+                         num_kv_heads, head_dim, dtype, workspace, workspace_bytes, stream,
+                         "paged_block_copy_ws launch");
 }
 
 }  // extern "C"

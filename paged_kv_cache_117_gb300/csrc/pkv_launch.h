@@ -140,8 +140,10 @@ cudaError_t launch_kv_write(const void *key, const void *value, void *k_cache,
                             int row_bytes, long long num_slots, unsigned *flags,
                             cudaStream_t stream);
 
+// counters: null (each copy CTA scans the pair list) or the caller's zeroed
+// [2, num_blocks] counter workspace (counting pass, copy, reset pass).
 cudaError_t launch_block_copy(void *k_cache, void *v_cache, const int64_t *pairs,
                               int num_pairs, long long block_bytes, int num_blocks,
-                              unsigned *flags, cudaStream_t stream);
+                              unsigned *counters, unsigned *flags, cudaStream_t stream);
 
 }  // namespace pkv

@@ -7,6 +7,7 @@ import os
 import sys
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -100,3 +101,72 @@ def test_prefix_manager_cost_is_reported():
     # holds its last token, which is always recomputed
     assert cost["cached_tokens_per_request_miss"] == 2048
     assert cost["cached_tokens_per_request_hit"] == 2048 + 256 - 16
+
+
+def _run_jobs(jobs):
+    import oracle.paged_ops as ops
+    return [bench.oracle_step(ops, j, j["k"].clone(), j["v"].clone()) for j in jobs]
+
+
+def test_oracle_jobs_reproduce_the_whole_batch():
+    """The CPU baseline splits a step by sequence into jobs on compact pools;
+    together they compute what the oracle computes on the whole batch."""
+    import oracle.paged_ops as ops
+    w = wl.scaled(wl.SHARED, 24, num_blocks=600)
+    w = bench.dataclasses.replace(w, lens_args=(3, 40, 8, 0, 9))
+    lens, tables, width, slots, pairs, setup = bench.build_shared_step(w, bench.OracleManager)
+    pairs = [tuple(p) for p in pairs.tolist()]
+    assert pairs, "the step should contain copy-on-write copies"
+    k, v = wl.make_pool(w)
+    ops.copy_blocks(k, v, setup)
+    q, key, value = wl.make_step_inputs(w)
+    kw, vw = k.clone(), v.clone()
+    ops.copy_blocks(kw, vw, pairs)
+    ops.write_kv(kw, vw, key, value, slots.tolist())
+    want = ops.attend(q, kw, vw, tables, lens, w.scale)
+    parts = bench.split_by_work(range(len(lens)), lens, 5)
+    assert len(parts) == 5 and sorted(s for p in parts for s in p) == list(range(len(lens)))
+    fetch = lambda ids: (k[ids], v[ids])
+    outs = _run_jobs(bench.oracle_jobs(w, "decode", parts, tables, lens, pairs, fetch, q, key,
+                                       value, slots.tolist()))
+    for part, out in zip(parts, outs):
+        assert torch.equal(out, want[part])
+
+
+def test_subchunk_jobs_reproduce_the_chunk():
+    """The reference arm splits one sequence's chunk by query rows; each
+    piece is the oracle's chunked call on a shorter sequence, and together
+    they give exactly the rows of the whole chunk."""
+    import oracle.paged_ops as ops
+    w = bench.dataclasses.replace(wl.PREFILL, num_seqs=3, num_blocks=64, lens_args=(40, 2))
+    lens, tables, width, slots, counts, qs, _ = bench.build_multiquery_step(
+        w, bench.OracleManager)
+    k, v = wl.make_pool(w)
+    T = qs[-1]
+    q = torch.randn((T, w.num_q_heads, w.head_dim),
+                    generator=torch.Generator().manual_seed(1)).to(w.dtype)
+    key, value = wl.make_rows(w, 0, T)
+    kw, vw = k.clone(), v.clone()
+    ops.write_kv(kw, vw, key, value, slots.tolist())
+    want = ops.attend_chunked(q, kw, vw, tables, lens, qs, w.scale)
+    fetch = lambda ids: (k[ids], v[ids])
+    for seq in range(len(lens)):
+        jobs = bench.subchunk_jobs(w, seq, lens, tables, counts, qs, fetch, q, key, value,
+                                   slots.tolist(), 4)
+        assert 1 < len(jobs) <= 4
+        got = torch.cat(_run_jobs(jobs))
+        assert torch.equal(got, want[qs[seq]:qs[seq + 1]])
+
+
+def test_oracle_pool_reports_the_workers_it_used():
+    w = wl.TINY
+    lens, tables, width, slots = bench.build_metadata(w, manager="oracle")
+    k, v = wl.make_pool(w)
+    q, key, value = wl.make_step_inputs(w)
+    pool = bench.OraclePool(3)
+    try:
+        cpu = bench.cpu_baseline_decode(pool, w, lens, tables, width, [],
+                                        lambda ids: (k[ids], v[ids]), q, key, value, slots)
+    finally:
+        pool.close()
+    assert cpu["cores"] == 3 and cpu["value"] > 0 and cpu["kind"] == "oracle"

@@ -182,6 +182,24 @@ def test_copy_validation(lib):
     assert f(fake(0), fake(1), fake(2), 0, 8, 16, 2, 128, BF16, None) == OK
 
 
+def test_copy_ws_validation(lib):
+    """paged_block_copy_ws: the counter workspace is checked on the host (present,
+    large enough, aligned, apart from the pools and the pairs) before any launch."""
+    f = lib.paged_block_copy_ws
+    assert lib.paged_block_copy_workspace_bytes(8) == 256
+    assert lib.paged_block_copy_workspace_bytes(40_000) == 320_000
+    assert lib.paged_block_copy_workspace_bytes(0) == ctypes.c_size_t(-1).value
+    ws = fake(5)
+    args = lambda **kw: [kw.get("k", fake(0)), fake(1), fake(2), kw.get("P", 3), 8, 16, 2, 128,
+                         BF16, kw.get("ws", ws), kw.get("n", 256), None]
+    assert f(*args(ws=None)) == WS
+    assert f(*args(n=255)) == WS
+    assert f(*args(ws=ws + 16)) == ALIGN
+    assert f(*args(ws=fake(0) + 256)) == ALIAS       # inside the K pool
+    assert f(*args(k=None)) == NULL
+    assert f(*args(P=0)) == OK                        # nothing to copy: no launch
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="CUDA library not found"):
         pkv.load(str(tmp_path / "missing.so"))

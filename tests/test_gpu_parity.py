@@ -287,6 +287,59 @@ def test_conflicting_copy_pairs_are_skipped_and_flagged():
     assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr)
 
 
+@pytest.mark.parametrize("with_ws", [False, True])
+def test_copy_4096_pairs_bitexact(with_ws):
+    """A long pair list (4,096 copies in one call, as a scheduler moving many
+    sequences would make): the whole pool equals the oracle's after the copy,
+    with the scan check and with the counter workspace; the workspace is all
+    zero again afterwards, ready for the next call."""
+    import oracle.paged_ops as ops
+    import paged_kv_cache_117_gb300 as pkv
+    g = torch.Generator().manual_seed(12)
+    N, B, H, D = 10_000, 16, 2, 64
+    k = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(N, generator=g).tolist()
+    pairs = [(perm[i], perm[4096 + i]) for i in range(4096)]
+    pairs[7] = (pairs[7][1], pairs[7][1])          # a block copied onto itself clashes with none
+    kr, vr = k.clone(), v.clone()
+    ops.copy_blocks(kr, vr, pairs)
+    kd, vd = k.cuda(), v.cuda()
+    ws = pkv.block_copy_workspace(kd) if with_ws else None
+    pt = gh.pairs_tensor(pairs).cuda()
+    for _ in range(2):                             # the second call finds the workspace reset
+        pkv.paged_block_copy(kd, vd, pt, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr)
+    assert _flags() == 0
+    if with_ws:
+        assert ws.numel() >= N * 8 and int(ws.count_nonzero()) == 0
+
+
+def test_conflicting_copy_pairs_with_workspace():
+    """The counter check finds the same conflicts as the scan, and leaves the
+    workspace zeroed."""
+    import oracle.paged_ops as ops
+    import paged_kv_cache_117_gb300 as pkv
+    g = torch.Generator().manual_seed(11)
+    N, B, H, D = 64, 16, 2, 128
+    k = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((N, B, H, D), generator=g).to(torch.bfloat16)
+    pairs = [(1, 10), (2, 11), (3, 10),      # dst 10 twice: both skipped
+             (4, 12), (12, 13),              # 12 is a dst and a src: (4, 12) skipped
+             (5, 20), (6, 21), (30, 30),     # clean; a self copy is clean too
+             (7, 99)]                        # out of the pool: skipped, range-flagged
+    kr, vr = k.clone(), v.clone()
+    ops.copy_blocks(kr, vr, [(2, 11), (12, 13), (5, 20), (6, 21)])
+    kd, vd = k.cuda(), v.cuda()
+    ws = pkv.block_copy_workspace(kd)
+    pkv.paged_block_copy(kd, vd, gh.pairs_tensor(pairs).cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert _flags() == pkv.FLAG_PAIR_CONFLICT | pkv.FLAG_PAIR_RANGE
+    assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr)
+    assert int(ws.count_nonzero()) == 0
+
+
 def test_empty_calls_launch_nothing():
     import paged_kv_cache_117_gb300 as pkv
     k = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
