@@ -43,7 +43,9 @@ METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 UNIT = "GB/s"
 FLUSH_BYTES = 256 << 20
 TABLE_WIDTH_TOKENS = {"tiny": 32, "opt13b": 2048, "llama8b": 8192, "qwen72b": 8192,
-                      "shared": 2048, "beam": 2048, "prefill": 8192, "prefix": 4096}
+                      "shared": 2048, "beam": 2048, "prefill": 8192, "prefix": 4096,
+                      "mixed": 8192}
+MULTIQUERY = ("chunked", "prefix", "mixed")   # workloads of several query rows per sequence
 SHARING = ("shared", "beam")   # workloads whose sequences share blocks
 
 
@@ -307,6 +309,18 @@ def build_multiquery_step(w, manager=None):
         return lens, tables, width, slots, counts, qs, desc
     prior, _ = wl.chunk_plan(w)
     lens, tables, width, slots, counts, qs = build_chunked_step(w, manager)
+    if w.lens_kind == "mixed":
+        n_dec, median, sigma, lo, hi, n_chunk, chunk, mx = w.lens_args
+        dec_tokens = sum(lens[:n_dec])
+        desc = (f"{w.name}: a continuous-batching step of {n_dec} decode sequences (lognormal "
+                f"lengths, median {median:g}, sigma {sigma:g}, clipped to [{lo}, {hi}]; "
+                f"{dec_tokens} tokens) and {n_chunk} prompt chunks of {chunk} tokens after "
+                f"0..{mx} cached chunks each (cached tokens {min(prior[n_dec:])}.."
+                f"{max(prior[n_dec:])}), {w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim "
+                f"{w.head_dim}, {str(w.dtype).replace('torch.', '')}, block {w.block_size}, "
+                f"{w.num_blocks}-block pool, blocks scattered by a seeded permutation, table "
+                f"width {width}, q/K/V ~ N(0,1)")
+        return lens, tables, width, slots, counts, qs, desc
     return lens, tables, width, slots, counts, qs, chunked_desc(w, width, prior, counts)
 
 
@@ -1060,6 +1074,23 @@ def run_native_chunked(a, world, rank, local):
     out = torch.empty((T, w.num_q_heads, w.head_dim), dtype=w.dtype, device=dev)
     flush = L2Flush(dev)
     flops = chunked_flops(w, lens, counts)
+    # a mixed batch goes through paged_attention_mixed: decode rows on the
+    # decode kernel, chunks on the tensor cores
+    mixed = w.lens_kind == "mixed"
+    ws = None
+    if mixed:
+        ws = torch.empty(max(16, pkv.paged_attention_workspace_bytes(
+            len(lens), w.num_q_heads, w.head_dim, width * w.block_size, w.partition_tokens)),
+            dtype=torch.uint8, device=dev)
+
+    def attend(o, qq, tb, ln, qsx, single=False):
+        if mixed and not single:
+            pkv.paged_attention_mixed(o, qq, k, v, tb, ln, qsx, w.scale, max_query_len=maxq,
+                                      p_format=a.p_format, partition_tokens=w.partition_tokens,
+                                      workspace=ws)
+        else:
+            pkv.paged_attention_chunked(o, qq, k, v, tb, ln, qsx, w.scale, max_query_len=maxq,
+                                        p_format=a.p_format)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -1077,8 +1108,7 @@ def run_native_chunked(a, world, rank, local):
         pkv.paged_kv_write(key, value, k, v, slots)
         if d0 is not None:
             d0.record(stream)
-        pkv.paged_attention_chunked(out, q, k, v, tab, lens_t, qs_t, w.scale, max_query_len=maxq,
-                                    p_format=a.p_format)
+        attend(out, q, tab, lens_t, qs_t)
         if d1 is not None:
             d1.record(stream)
 
@@ -1126,8 +1156,7 @@ def run_native_chunked(a, world, rank, local):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         pkv.paged_kv_write(e_key, e_val, k, v, e_slots)
-        pkv.paged_attention_chunked(out, e_q, k, v, e_tab, e_lens, e_qs, w.scale,
-                                    max_query_len=maxq, p_format=a.p_format)
+        attend(out, e_q, e_tab, e_lens, e_qs)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -1148,6 +1177,41 @@ def run_native_chunked(a, world, rank, local):
     peak, kind = peak_bf16()
     achieved = flops / (dec_ms * 1e-3) / 1e12
     value_tf = world * flops / (step_ms * 1e-3) / 1e12
+    roof = {"kernel": "paged_attention_chunked (tcgen05)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{kind} bf16_tflops (burst)", "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": measured_traffic(w.name, 0, "chunked_kernel_prefill.md", CHUNKED_SOURCES)}
+    extra = {}
+    if mixed:
+        # the same batch in one paged_attention_chunked launch, for comparison
+        sev = [(ev(), ev()) for _ in range(K)]
+        host_head_start()
+        for e0, e1 in sev:
+            flush()
+            e0.record(stream)
+            attend(out, q, tab, lens_t, qs_t, single=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        single_ms = sum(e0.elapsed_time(e1) for e0, e1 in sev) / K
+        # the call's floor: the decode rows' bytes at the HBM peak plus the
+        # chunks' flops at the bf16 peak
+        n_dec = w.lens_args[0]
+        hbm, hkind = peak_hbm()
+        dec_bytes = algorithmic_bytes(w, lens[:n_dec], width, w.partition_tokens,
+                                      out.element_size())["attention"]
+        ch_flops = chunked_flops(w, lens[n_dec:], counts[n_dec:])
+        floor_ms = 1e3 * (dec_bytes / (hbm * 1e9) + ch_flops / (peak * 1e12))
+        roof = {"kernel": "paged_attention_mixed (decode rows: decode kernel, HBM; chunks: "
+                          "tcgen05 kernel, tensor)", "bound": "hbm+tensor",
+                "achieved": round(floor_ms / dec_ms, 4), "peak": 1.0,
+                "peak_kind": f"time floor {floor_ms * 1e3:.1f} us = decode rows' "
+                             f"{dec_bytes} B at the {hkind} {hbm} GB/s + chunks' {ch_flops} "
+                             f"FLOP at the {kind} {peak} TFLOP/s", "unit": "floor / time",
+                "frac": round(floor_ms / dec_ms, 4), "traffic": None}
+        extra = {"single_chunked_call_ms": round(single_ms, 4),
+                 "speedup_vs_single_chunked_call": round(single_ms / dec_ms, 3),
+                 "decode_rows": n_dec, "decode_bytes": dec_bytes, "chunk_flops": ch_flops}
     return {
         "metric": CHUNK_METRIC, "value": round(value_tf, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": max(3, a.warmup), "ms_per_step": round(step_ms, 4),
@@ -1159,16 +1223,12 @@ def run_native_chunked(a, world, rank, local):
         "tokens_per_s": round(world * T / (step_ms * 1e-3), 1),
         "attention_ms": round(dec_ms, 4),
         "flops_per_step": flops,
-        "roofline": {"kernel": "paged_attention_chunked (tcgen05)", "bound": "tensor",
-                     "achieved": round(achieved, 1), "peak": peak,
-                     "peak_kind": f"{kind} bf16_tflops (burst)", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": measured_traffic(w.name, 0, "chunked_kernel_prefill.md",
-                                                 CHUNKED_SOURCES)},
+        "roofline": roof,
+        **extra,
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": sum(sizes),
                 "d2h_bytes_per_step": h_out.numel() * h_out.element_size()},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (4 if mixed else 2) * K,
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
         "cpu_baseline": cpu,
@@ -1376,7 +1436,8 @@ def run_reference_chunked(a, world, rank, local):
         return None
     w = wl.WORKLOADS[a.workload]
     lens, tables, width, slots, counts, qs, desc = build_multiquery_step(w, OracleManager)
-    seq = min(range(len(lens)), key=lambda s: lens[s])
+    multi = [s for s in range(len(lens)) if counts[s] > 1] or list(range(len(lens)))
+    seq = min(multi, key=lambda s: lens[s])
     fetch = host_pool_fetch(w, sorted(set(tables[seq])), w.seed + 2000)
     T = qs[-1]
     g = torch.Generator().manual_seed(w.seed + 3000)
@@ -1406,7 +1467,7 @@ def run_reference_chunked(a, world, rank, local):
 def main():
     a = parse_args()
     world, rank, local = dist_init()
-    chunked = wl.WORKLOADS[a.workload].lens_kind in ("chunked", "prefix")
+    chunked = wl.WORKLOADS[a.workload].lens_kind in MULTIQUERY
     if chunked and (a.seqs is not None or a.context is not None):
         raise SystemExit("--seqs / --context apply to the decode workloads of independent "
                          "sequences (tiny, opt13b, llama8b, qwen72b)")

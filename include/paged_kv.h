@@ -307,6 +307,47 @@ pkv_status paged_attention_chunked(
     float scale, pkv_p_format p_format, pkv_stream_t stream);
 
 /*
+ * paged_attention_mixed -- paged_attention_chunked for a batch that mixes
+ * decode tokens with prompt chunks, as continuous batching builds one step
+ * ("Paging the KV Cache Like an OS", continuous batching: the scheduler puts
+ * every waiting decode in the step before it fills the rest of the token
+ * budget with prefill chunks).
+ *
+ * Same arguments, layouts and result as paged_attention_chunked, plus the
+ * decode attention's partition size and workspace.  A sequence with exactly
+ * one query row (n_s = 1: a decode token) goes to the decode kernel (the one
+ * paged_attention_decode runs: the block table walked in partitions, each
+ * K/V block read once for the whole query group, CUDA cores and warp-level
+ * MMAs), its query and output rows found through query_start; the sequences
+ * with more rows go to the tensor-core kernel of paged_attention_chunked,
+ * which skips the single-row ones.  In one chunked launch a decode row fills
+ * 1 of the 128 rows of its MMA tile; here it costs what a decode step costs.
+ *
+ *   partition_tokens  as paged_attention_decode (multiple of block_size;
+ *                     0 = one partition per sequence)
+ *   workspace         DEVICE memory of at least
+ *                     paged_attention_workspace_bytes(num_seqs, num_q_heads,
+ *                     head_dim, max_blocks * block_size, partition_tokens)
+ *                     bytes, 256-byte aligned, no initial contents needed;
+ *                     calls that share one must not overlap in time.
+ *
+ * Two or three kernels in stream order (the decode work list, the decode
+ * pass, then the chunked pass when max_query_len > 1); they write disjoint
+ * rows of out.  Every argument is checked before the first launch; errors as
+ * paged_attention_chunked and paged_attention_decode.  A single-row sequence
+ * whose row lies outside [0, num_tokens) or whose context length is below 1
+ * is skipped and flagged (PKV_FLAG_LEN_RANGE).
+ */
+pkv_status paged_attention_mixed(
+    void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
+    const void *v_cache, pkv_dtype dtype, const int32_t *block_tables,
+    int max_blocks, const int32_t *context_lens, const int32_t *query_start,
+    int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, pkv_p_format p_format, int partition_tokens, void *workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * Scratch bytes paged_attention_decode needs, with
  * P = ceil(max_context / partition_tokens) (P = 1 when partition_tokens is 0)
  * and max_context the capacity of one block-table row (max_blocks *

@@ -8,7 +8,7 @@ from .binding import (  # noqa: F401
     FLAG_BLOCK_RANGE, FLAG_LEN_RANGE, FLAG_PAIR_CONFLICT, FLAG_PAIR_RANGE, FLAG_SLOT_RANGE, FLAG_TIMEOUT, FLAG_V_RANGE,
     BlockManager, PrefixCache, chain_keys, sha256, EXPORTED_SYMBOLS, NOALLOC_SCRATCH_BYTES, PkvError, load,
     paged_attention_decode, paged_attention_decode_noalloc, paged_attention_decode_append,
-    paged_attention_chunked,
+    paged_attention_chunked, paged_attention_mixed,
     paged_attention_workspace_bytes, paged_block_copy, paged_kv_write, read_device_flags,
     block_copy_workspace, paged_block_copy_workspace_bytes,
 )

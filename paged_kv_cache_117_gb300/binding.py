@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "paged_attention_decode_noalloc",
     "paged_attention_decode_append",
     "paged_attention_chunked",
+    "paged_attention_mixed",
     "pkv_pc_create",
     "pkv_pc_add_sequence",
     "pkv_pc_append",
@@ -105,6 +106,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.paged_attention_chunked.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, vp, ci, ci, ci,
                                             ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
     lib.paged_attention_chunked.restype = ci
+    lib.paged_attention_mixed.argtypes = [vp, ci, vp, vp, vp, ci, vp, ci, vp, vp, ci, ci, ci,
+                                          ci, ci, ci, ci, ci, ctypes.c_float, ci, ci, vp, cs, vp]
+    lib.paged_attention_mixed.restype = ci
     lib.pkv_bm_create.argtypes = [ci, ci, vp]
     lib.pkv_bm_create.restype = vp
     lib.pkv_bm_destroy.argtypes = [vp]
@@ -353,6 +357,40 @@ def paged_attention_chunked(out, q, k_cache, v_cache, block_tables, context_lens
         _ptr(context_lens), _ptr(query_start), S, T, int(max_query_len), Hq, Hkv, D, B, N,
         float(scale), P_FORMATS.get(p_format, -1), _stream(stream))
     _check("paged_attention_chunked", st)
+    return out
+
+
+def paged_attention_mixed(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                          scale, max_query_len=None, p_format="hilo", partition_tokens=512,
+                          workspace=None, stream=None):
+    """paged_attention_chunked for a batch that mixes decode tokens with
+    prompt chunks: the sequences with one query row run on the decode kernel
+    (rows found through query_start), the others on the tensor-core kernel.
+    A workspace tensor is allocated by torch when none is given."""
+    _need_cuda("paged_attention_mixed", out, q, k_cache, v_cache, block_tables, context_lens,
+               query_start)
+    N, B, Hkv, D = _cache_dims(k_cache)
+    T, Hq, _ = (int(x) for x in q.shape)
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32
+            or query_start.dtype != torch.int32):
+        raise ValueError("block_tables, context_lens and query_start must be int32")
+    S = int(context_lens.shape[0])
+    if int(query_start.shape[0]) != S + 1:
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if S else 0
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None and S:
+        need = paged_attention_workspace_bytes(S, Hq, D, max_blocks * B, partition_tokens)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().paged_attention_mixed(
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _DTYPE_CODE.get(k_cache.dtype, -1), _ptr(block_tables), max_blocks, _ptr(context_lens),
+        _ptr(query_start), S, T, int(max_query_len), Hq, Hkv, D, B, N, float(scale),
+        P_FORMATS.get(p_format, -1), int(partition_tokens), _ptr(workspace), ws_bytes,
+        _stream(stream))
+    _check("paged_attention_mixed", st)
     return out
 
 

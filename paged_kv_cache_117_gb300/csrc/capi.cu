@@ -260,7 +260,8 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int block_size, int num_blocks, float scale, int partition_tokens,
                        void *workspace, size_t workspace_bytes, pkv_stream_t stream,
-                       const char *what) {
+                       const char *what, const int32_t *query_start = nullptr,
+                       int num_tokens = 0) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks <= 0 || partition_tokens < 0)
     return PKV_ERR_RANGE;
@@ -292,9 +293,14 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
   if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
 
   const size_t pool = (size_t)num_blocks * block_size * num_kv_heads * head_dim * 2;
-  const size_t out_sz = (size_t)num_seqs * num_q_heads * head_dim * dtype_bytes(out_dtype);
-  const size_t q_sz = (size_t)num_seqs * num_q_heads * head_dim * 2;
+  // q and out rows: one per sequence, or (a mixed batch) num_tokens
+  const size_t nrows = query_start ? (size_t)num_tokens : (size_t)num_seqs;
+  const size_t out_sz = nrows * num_q_heads * head_dim * dtype_bytes(out_dtype);
+  const size_t q_sz = nrows * num_q_heads * head_dim * 2;
   const size_t tab_sz = (size_t)num_seqs * max_blocks * 4;
+  if (query_start && (overlap(workspace, need, query_start, (size_t)(num_seqs + 1) * 4) ||
+                      overlap(out, out_sz, query_start, (size_t)(num_seqs + 1) * 4)))
+    return PKV_ERR_ALIAS;
   if (overlap(k_cache, pool, v_cache, pool) || overlap(out, out_sz, q, q_sz) ||
       overlap(out, out_sz, k_cache, pool) || overlap(out, out_sz, v_cache, pool) ||
       overlap(out, out_sz, block_tables, tab_sz) ||
@@ -354,6 +360,8 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
   p.value_new = value_new;
   p.k_pool = key_new ? k_cache : nullptr;
   p.v_pool = key_new ? v_cache : nullptr;
+  p.query_start = query_start;
+  p.num_tokens = num_tokens;
 
   int launches = 0;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -399,14 +407,19 @@ pkv_status paged_attention_decode_append(void *out, pkv_dtype out_dtype, const v
                      stream, "paged_attention_decode_append launch");
 }
 
-pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q,
-                                   const void *k_cache, const void *v_cache, pkv_dtype dtype,
-                                   const int32_t *block_tables, int max_blocks,
-                                   const int32_t *context_lens, const int32_t *query_start,
-                                   int num_seqs, int num_tokens, int max_query_len,
-                                   int num_q_heads, int num_kv_heads, int head_dim,
-                                   int block_size, int num_blocks, float scale,
-                                   pkv_p_format p_format, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Multi-query attention.  skip_single: the sequences with one query row are
+// left out (a mixed batch whose decode rows go to the decode kernel).
+pkv_status chunked_impl(void *out, pkv_dtype out_dtype, const void *q, const void *k_cache,
+                        const void *v_cache, pkv_dtype dtype, const int32_t *block_tables,
+                        int max_blocks, const int32_t *context_lens,
+                        const int32_t *query_start, int num_seqs, int num_tokens,
+                        int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int num_blocks, float scale, pkv_p_format p_format,
+                        pkv_stream_t stream, int skip_single, bool validate_only,
+                        const char *what) {
   if (p_format != PKV_P_HILO && p_format != PKV_P_F16) return PKV_ERR_DTYPE;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
@@ -439,6 +452,7 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
       overlap(out, out_sz, context_lens, (size_t)num_seqs * 4) ||
       overlap(out, out_sz, query_start, (size_t)(num_seqs + 1) * 4))
     return PKV_ERR_ALIAS;
+  if (validate_only) return PKV_OK;
 
   CUtensorMap kmap, vmap, qmap;
   // chunked: a whole block (up to 32 tokens) a box -- fewer, larger TMA boxes
@@ -483,6 +497,7 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
   p.num_qtiles = (int)qtiles;
   p.num_qpairs = (int)((qtiles + 1) / 2);
   p.p_format = (int)p_format;
+  p.skip_single = skip_single;
   p.max_query_len = max_query_len;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -491,7 +506,56 @@ pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q
   const cudaError_t e =
       dtype == PKV_BF16 ? pkv::launch_chunked_bf16(qmap, kmap, vmap, p, head_dim, block_size, st)
                         : pkv::launch_chunked_f16(qmap, kmap, vmap, p, head_dim, block_size, st);
-  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention_chunked launch");
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, what);
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_attention_chunked(void *out, pkv_dtype out_dtype, const void *q,
+                                   const void *k_cache, const void *v_cache, pkv_dtype dtype,
+                                   const int32_t *block_tables, int max_blocks,
+                                   const int32_t *context_lens, const int32_t *query_start,
+                                   int num_seqs, int num_tokens, int max_query_len,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, float scale,
+                                   pkv_p_format p_format, pkv_stream_t stream) {
+  return chunked_impl(out, out_dtype, q, k_cache, v_cache, dtype, block_tables, max_blocks,
+                      context_lens, query_start, num_seqs, num_tokens, max_query_len,
+                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                      p_format, stream, 0, false, "paged_attention_chunked launch");
+}
+
+pkv_status paged_attention_mixed(void *out, pkv_dtype out_dtype, const void *q,
+                                 const void *k_cache, const void *v_cache, pkv_dtype dtype,
+                                 const int32_t *block_tables, int max_blocks,
+                                 const int32_t *context_lens, const int32_t *query_start,
+                                 int num_seqs, int num_tokens, int max_query_len,
+                                 int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, float scale,
+                                 pkv_p_format p_format, int partition_tokens, void *workspace,
+                                 size_t workspace_bytes, pkv_stream_t stream) {
+  // every argument of both halves is checked before anything is launched
+  pkv_status st = chunked_impl(out, out_dtype, q, k_cache, v_cache, dtype, block_tables,
+                               max_blocks, context_lens, query_start, num_seqs, num_tokens,
+                               max_query_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                               num_blocks, scale, p_format, stream, 1, true,
+                               "paged_attention_mixed launch");
+  if (st != PKV_OK || num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return st;
+  if (num_seqs > 65535) return PKV_ERR_RANGE;
+  if (!workspace) return PKV_ERR_WORKSPACE;
+  // the decode rows (sequences with one query row), then the chunks; the two
+  // kernels write disjoint rows of out and only read the pool
+  st = decode_impl(out, out_dtype, q, nullptr, nullptr, const_cast<void *>(k_cache),
+                   const_cast<void *>(v_cache), dtype, block_tables, max_blocks, context_lens,
+                   num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                   partition_tokens, workspace, workspace_bytes, stream,
+                   "paged_attention_mixed decode launch", query_start, num_tokens);
+  if (st != PKV_OK || max_query_len < 2) return st;
+  return chunked_impl(out, out_dtype, q, k_cache, v_cache, dtype, block_tables, max_blocks,
+                      context_lens, query_start, num_seqs, num_tokens, max_query_len,
+                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                      p_format, stream, 1, false, "paged_attention_mixed chunked launch");
 }
 
 pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear, pkv_stream_t stream) {

@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
       const int q = ord_s[r];
       const int a = qs_s[q], b = qs_s[q + 1], n = b - a;
       const bool valid = a >= 0 && n >= 0 && b <= p.num_tokens && n <= p.max_query_len;
-      cnt_s[r] = (!valid ? 1 : ((n + TQ - 1) / TQ + 1) / 2) * p.num_kv_heads;
+      const int pairs = !valid ? 1 : (p.skip_single && n == 1 ? 0 : ((n + TQ - 1) / TQ + 1) / 2);
+      cnt_s[r] = pairs * p.num_kv_heads;
     }
     if (tid == 0) red[32] = -1;
     __syncthreads();
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   fence_proxy_async_smem();   // the scratch is a TMA destination later
   const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
   const int n = q1 - q0;
+  if (p.skip_single && n == 1) return;   // a decode row: the decode kernel's
   int L = p.context_lens[s];
   if (q0 < 0 || n < 0 || q1 > p.num_tokens || n > p.max_query_len || L < n) {
     if (tid == 0 && pr_rev == 0 && kvh == 0) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);

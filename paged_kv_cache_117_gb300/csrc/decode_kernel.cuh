@@ -158,10 +158,24 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   auto cls = [=](int nb) {
     return nb > PB ? plan_bucket(nb % PB, PB, nbk) : nbk + plan_bucket(nb, PB + 1, nbk);
   };
+  // a mixed batch: only the sequences with exactly one query row are this
+  // kernel's; one whose row lies outside q, or whose context cannot hold it,
+  // is flagged and skipped
+  auto mine = [&](int s, bool flag) -> bool {
+    if (!p.query_start) return true;
+    const int a = __ldg(p.query_start + s), b = __ldg(p.query_start + s + 1);
+    if (b - a != 1) return false;
+    if (a < 0 || b > p.num_tokens || __ldg(p.context_lens + s) < 1) {
+      if (flag) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
+      return false;
+    }
+    return true;
+  };
   slot[tid] = 0;
   __syncthreads();
   int nf = 0;
   for (int s = s0; s < s1; ++s) {
+    if (!mine(s, true)) continue;
     const int L0 = __ldg(p.context_lens + s);
     if (L0 < 0 || L0 > cap) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
     const int nb = (clamp_len(L0, cap) + Bs - 1) / Bs;
@@ -199,6 +213,7 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   slot[tid] = total_f + xp - np + (wid ? wsum_p[wid - 1] : 0);
   __syncthreads();
   for (int s = s0; s < s1; ++s) {
+    if (!mine(s, false)) continue;
     const int L = clamp_len(__ldg(p.context_lens + s), cap);
     const int nb = (L + Bs - 1) / Bs;
     const int F = nb > PB ? nb / PB : 0;
@@ -224,6 +239,7 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
 // streams and its slice of the block table.
 struct WarpLoads {
   int s;            // sequence
+  int row;          // its row of q and out
   int part;         // partition
   int hc;           // KV head x query-head chunk index
   int L;            // context length (clamped)
@@ -251,6 +267,7 @@ __device__ __forceinline__ void decode_unit_loads(WarpLoads &wl, const DecodePar
   const int jb = part * p.part_blocks;
   const int je = min(nb, jb + p.part_blocks);
   wl.s = s;
+  wl.row = p.query_start ? __ldg(p.query_start + s) : s;
   wl.part = part;
   wl.hc = hc;
   wl.L = L;
@@ -278,7 +295,7 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qb)[D / 16][NH][2], cons
   const int g0 = gc * HEADS;
   const int gcount = min(HEADS, p.group - g0);
   const T *qp = static_cast<const T *>(p.q) +
-                ((size_t)wl.s * p.num_q_heads + wl.kvh * p.group + g0) * D;
+                ((size_t)wl.row * p.num_q_heads + wl.kvh * p.group + g0) * D;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks)
 #pragma unroll
@@ -417,7 +434,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
     const int g0 = gc * C::HEADS;
     const int gcount = min(C::HEADS, p.group - g0);
     const int hq0 = kvh * p.group + g0;
-    const size_t out_base = ((size_t)s * p.num_q_heads + hq0) * D;
+    const size_t out_base = ((size_t)cur.row * p.num_q_heads + hq0) * D;
 
     // Appending: the warp whose blocks include position L - 1 fetches this
     // step's K (lanes 0..D/8-1) or V (the next D/8 lanes) row piece now, so

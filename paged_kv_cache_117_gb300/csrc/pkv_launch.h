@@ -73,6 +73,12 @@ struct DecodeParams {
   const void *value_new = nullptr;
   void *k_pool = nullptr;
   void *v_pool = nullptr;
+  // A mixed batch (null: row s of q and out is sequence s): sequence s owns
+  // rows query_start[s] .. query_start[s + 1] - 1 of q and out, and only the
+  // sequences with exactly one row are this kernel's (the others are left to
+  // the chunked kernel).
+  const int32_t *query_start = nullptr;
+  int num_tokens = 0;            // rows of q and out when query_start is set
 };
 
 // Launch the work-list pass and the decode pass for one cache dtype /
@@ -103,6 +109,7 @@ struct ChunkedParams {
   int num_qpairs;                // ceil(num_qtiles / 2): query tiles go two to a CTA
   int compact = 0;               // the grid lists only existing units (set at launch)
   int p_format;                  // pkv_p_format
+  int skip_single = 0;           // sequences with one query row are left to the decode kernel
   int max_query_len;
   int num_blocks;
   float scale_log2;

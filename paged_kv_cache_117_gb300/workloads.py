@@ -30,6 +30,9 @@ The five workloads follow the shapes the pages use for their examples:
 * ``prefix``   -- prefix caching (same page, section 2.4): 32 requests over 2
                   cached 2,048-token system prompts, each prefilling its own
                   256-token question.
+* ``mixed``    -- a continuous-batching step (same page, continuous batching):
+                  the ``llama8b`` decode batch plus 8 prompt chunks of 512
+                  tokens.
 
 The pages measure on ShareGPT/Alpaca traces; none is used or reproduced here.
 Lengths come from the seeded distributions below instead.
@@ -55,7 +58,7 @@ class Workload:
     dtype: torch.dtype
     partition_tokens: int          # 0 = one partition per sequence
     seed: int
-    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam" | "chunked" | "prefix"
+    lens_kind: str                 # "fixed" | "uniform" | "lognormal" | "shared" | "beam" | "chunked" | "prefix" | "mixed"
     lens_args: tuple = field(default_factory=tuple)
 
     @property
@@ -107,7 +110,16 @@ PREFILL = Workload("prefill", 16, 32, 8, 128, 16, 16_384, torch.bfloat16, 0, 124
 PREFIX = Workload("prefix", 32, 32, 8, 128, 16, 16_384, torch.bfloat16, 0, 125,
                   "prefix", (2, 2048, 256))
 
-WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM, PREFILL, PREFIX)}
+# A continuous-batching step ("Paging the KV Cache Like an OS", continuous
+# batching: every waiting decode goes into the step, prefill chunks fill the
+# rest of the token budget): the Llama-3.1-8B decode batch (256 sequences,
+# lognormal lengths as in ``llama8b``) plus 8 prompt chunks of 512 tokens
+# after 0..7 cached chunks each.
+MIXED = Workload("mixed", 264, 32, 8, 128, 16, 40_000, torch.bfloat16, 768, 126,
+                 "mixed", (256, 1024.0, 0.8, 16, 8192, 8, 512, 7))
+
+WORKLOADS = {w.name: w for w in (TINY, OPT13B, LLAMA8B, QWEN72B, SHARED, BEAM, PREFILL, PREFIX,
+                                 MIXED)}
 
 
 def scaled(w: Workload, num_seqs: int, max_len: Optional[int] = None,
@@ -232,7 +244,15 @@ def pad_tables(tables: Sequence[Sequence[int]], width: Optional[int] = None,
 
 def chunk_plan(w: Workload):
     """(prior tokens, this step's query tokens) per sequence of a chunked
-    prefill workload."""
+    prefill workload, or of a mixed one (decode sequences first: L_s - 1
+    earlier tokens and one new token each; then the prompt chunks)."""
+    if w.lens_kind == "mixed":
+        n_dec, median, sigma, lo, hi, n_chunk, chunk, max_prior = w.lens_args
+        g = _gen(w.seed)
+        z = torch.randn(n_dec, generator=g, dtype=torch.float64)
+        lens = [int(min(max(round(float(x)), lo), hi)) for x in torch.exp(math.log(median) + sigma * z)]
+        prior = (torch.randint(0, max_prior + 1, (n_chunk,), generator=g) * chunk).tolist()
+        return [L - 1 for L in lens] + [int(x) for x in prior], [1] * n_dec + [chunk] * n_chunk
     chunk, max_prior = w.lens_args
     g = _gen(w.seed)
     prior = (torch.randint(0, max_prior + 1, (w.num_seqs,), generator=g) * chunk).tolist()

@@ -160,6 +160,36 @@ def test_chunked_validation(lib):
     assert chunked(lib, S=0) == OK
 
 
+def mixed(lib, **kw):
+    a = dict(out=fake(0), out_dt=F32, q=fake(1), k=fake(2), v=fake(3), dt=BF16, tab=fake(4),
+             max_blocks=4, lens=fake(5), qs=fake(6), S=2, T=64, maxq=32, Hq=8, Hkv=2, D=128,
+             B=16, N=8, scale=0.1, pf=0, pt=32, ws=fake(7), ws_bytes=1 << 20)
+    a.update(kw)
+    return lib.paged_attention_mixed(a["out"], a["out_dt"], a["q"], a["k"], a["v"], a["dt"],
+                                     a["tab"], a["max_blocks"], a["lens"], a["qs"], a["S"],
+                                     a["T"], a["maxq"], a["Hq"], a["Hkv"], a["D"], a["B"],
+                                     a["N"], a["scale"], a["pf"], a["pt"], a["ws"],
+                                     a["ws_bytes"], None)
+
+
+def test_mixed_validation(lib):
+    """paged_attention_mixed checks the chunked half's arguments and the decode
+    half's (partition, workspace) before anything is launched."""
+    assert mixed(lib, q=None) == NULL
+    assert mixed(lib, qs=None) == NULL
+    assert mixed(lib, pf=2) == DTYPE
+    assert mixed(lib, B=4) == SHAPE                       # the chunked half needs blocks of 8+
+    assert mixed(lib, pt=24) == SHAPE                     # partition not a multiple of the block
+    assert mixed(lib, maxq=65) == RANGE
+    assert mixed(lib, ws=None) == WS
+    assert mixed(lib, ws_bytes=64) == WS
+    assert mixed(lib, ws=fake(7) + 16) == ALIGN
+    assert mixed(lib, ws=fake(0)) == ALIAS                # the workspace over the output
+    assert mixed(lib, out=fake(6)) == ALIAS               # the output over query_start
+    assert mixed(lib, T=0, maxq=0) == OK                  # nothing to do: no CUDA call
+    assert mixed(lib, S=0) == OK
+
+
 def test_write_validation(lib):
     f = lib.paged_kv_write
     assert f(None, fake(1), fake(2), fake(3), fake(4), 4, 8, 16, 2, 128, BF16, None) == NULL

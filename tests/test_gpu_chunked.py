@@ -20,7 +20,7 @@ def _w(Hq, Hkv, D, B, dtype=torch.bfloat16, N=400, seed=500):
 
 
 def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None, p_format="hilo",
-         v_spike=None):
+         v_spike=None, mixed=False, partition_tokens=64):
     import paged_kv_cache_117_gb300 as pkv
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
@@ -42,10 +42,14 @@ def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None, p_
     pkv.paged_kv_write(key.cuda(), val.cuda(), kd, vd,
                        torch.tensor(step.slots, dtype=torch.int64, device="cuda"))
     out = torch.full((T, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype, device="cuda")
-    pkv.paged_attention_chunked(out, q.cuda(), kd, vd, wl.pad_tables(step.tables, step.width).cuda(),
-                                torch.tensor(step.lens, dtype=torch.int32, device="cuda"),
-                                torch.tensor(step.query_start, dtype=torch.int32, device="cuda"),
-                                w.scale, max_query_len=max(counts), p_format=p_format)
+    args = (out, q.cuda(), kd, vd, wl.pad_tables(step.tables, step.width).cuda(),
+            torch.tensor(step.lens, dtype=torch.int32, device="cuda"),
+            torch.tensor(step.query_start, dtype=torch.int32, device="cuda"), w.scale)
+    if mixed:
+        pkv.paged_attention_mixed(*args, max_query_len=max(counts), p_format=p_format,
+                                  partition_tokens=partition_tokens)
+    else:
+        pkv.paged_attention_chunked(*args, max_query_len=max(counts), p_format=p_format)
     torch.cuda.synchronize()
     flags = pkv.read_device_flags(clear=True)
     if v_spike is not None:
@@ -55,6 +59,68 @@ def _run(w, prior, counts, out_dtype=torch.float32, poison=False, width=None, p_
     assert torch.equal(kd.cpu().view(torch.int16), k.view(torch.int16))
     assert torch.equal(vd.cpu().view(torch.int16), v.view(torch.int16))
     return gh.assert_close_to_oracle(out, ref, ATOL), step
+
+
+# ---- mixed batches: decode rows on the decode kernel, chunks on the tensor cores
+
+@pytest.mark.parametrize("pt", [0, 16, 64])
+def test_mixed_call_prefill_and_decode(pt):
+    # prompt chunks at various offsets, decode tokens (one at the very first
+    # position, one spanning several partitions), an idle sequence
+    _run(_w(8, 2, 128, 16), [0, 200, 511, 37, 1000, 64, 5, 0],
+         [130, 129, 1, 1, 256, 0, 3, 1], mixed=True, partition_tokens=pt)
+
+
+def test_mixed_call_decode_only_and_chunks_only():
+    _run(_w(8, 2, 128, 16), [0, 17, 300, 4000], [1, 1, 1, 1], mixed=True, width=300)
+    _run(_w(8, 2, 128, 16), [0, 300], [40, 2], mixed=True)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (16, 1), (40, 40), (64, 8)])
+def test_mixed_call_group_sizes(hq, hkv):
+    _run(_w(hq, hkv, 128, 16, N=500), [0, 150, 9, 77], [97, 1, 2, 1], mixed=True)
+
+
+def test_mixed_call_f16_cache_16bit_outputs_and_f16_p():
+    w = _w(8, 2, 64, 32, dtype=torch.float16)
+    _run(w, [0, 90, 33], [150, 1, 70], out_dtype=torch.float16, mixed=True)
+    _run(_w(8, 2, 128, 16), [0, 90, 5], [150, 1, 70], out_dtype=torch.bfloat16, mixed=True,
+         p_format="f16")
+
+
+def test_mixed_decode_rows_equal_the_decode_call():
+    """A decode row of a mixed batch is computed exactly as paged_attention_decode
+    computes it: the same kernel, partitions and merge order, so the rows are
+    bit-identical; the chunk rows are the chunked kernel's."""
+    import paged_kv_cache_117_gb300 as pkv
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = _w(32, 8, 128, 16, N=1200)
+    prior, counts = [900, 0, 3000, 64, 2000], [1, 200, 1, 1, 77]
+    step = gh.plan_chunked(w, prior, counts, None)
+    T = step.query_start[-1]
+    k, v = wl.make_pool(w, "cuda")
+    g = torch.Generator().manual_seed(9)
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=g).to(w.dtype).cuda()
+    key, val = wl.make_rows(w, 0, T, "cuda")
+    pkv.paged_kv_write(key, val, k, v, torch.tensor(step.slots, dtype=torch.int64, device="cuda"))
+    tab = wl.pad_tables(step.tables, step.width).cuda()
+    lens = torch.tensor(step.lens, dtype=torch.int32, device="cuda")
+    qs = torch.tensor(step.query_start, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, w.num_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    pkv.paged_attention_mixed(out, q, k, v, tab, lens, qs, w.scale, partition_tokens=256)
+    chunk = torch.empty_like(out)
+    pkv.paged_attention_chunked(chunk, q, k, v, tab, lens, qs, w.scale)
+    dec = [s for s, n in enumerate(counts) if n == 1]
+    rows = [step.query_start[s] for s in dec]
+    dout = torch.empty((len(dec), w.num_q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(dout, q[rows].contiguous(), k, v, tab[dec].contiguous(),
+                               lens[dec].contiguous(), w.scale, partition_tokens=256)
+    torch.cuda.synchronize()
+    assert pkv.read_device_flags(clear=True) == 0
+    assert torch.equal(out[rows], dout)
+    other = [r for r in range(T) if r not in rows]
+    assert torch.equal(out[other], chunk[other])
 
 
 def test_one_prompt_whole():
