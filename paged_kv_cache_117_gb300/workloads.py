@@ -77,7 +77,7 @@ class Workload:
 # seed = 117 + the workload's position in the list below (1-based)
 TINY = Workload("tiny", 4, 4, 4, 64, 4, 64, torch.bfloat16, 0, 118,
                 "fixed", (1, 6, 9, 17))
-OPT13B = Workload("opt13b", 64, 40, 40, 128, 16, 10_000, torch.float16, 512, 119,
+OPT13B = Workload("opt13b", 64, 40, 40, 128, 16, 10_000, torch.float16, 1024, 119,
                   "uniform", (128, 2048))
 LLAMA8B = Workload("llama8b", 256, 32, 8, 128, 16, 40_000, torch.bfloat16, 768, 120,
                    "lognormal", (1024.0, 0.8, 16, 8192))
