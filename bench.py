@@ -406,10 +406,13 @@ def sources_sha256(sources):
     return h.hexdigest()
 
 
-def measured_traffic(workload, partition_tokens, profile="decode_kernel_llama8b.md",
-                     sources=DECODE_SOURCES, kv_write=None):
-    """DRAM bytes per launch from a committed ncu summary, or None when it was
-    taken on another workload or the kernel's sources changed since."""
+def measured_traffic(workload, partition_tokens, profile=None, sources=DECODE_SOURCES,
+                     kv_write=None):
+    """DRAM bytes per launch from a committed ncu summary (by default the
+    decode kernel's on this workload, profiles/decode_kernel_<workload>.md),
+    or None when there is none, it was taken on another workload or partition
+    size, or the kernel's sources changed since."""
+    profile = profile or f"decode_kernel_{workload}.md"
     try:
         text = open(os.path.join(ROOT, "profiles", profile)).read()
         kv = dict(line.split(": ", 1) for line in text.splitlines()
