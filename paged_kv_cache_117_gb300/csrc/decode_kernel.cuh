@@ -66,7 +66,7 @@ constexpr int DECODE_WARPS = 4;
 constexpr int SMEM_PER_SM = 228 * 1024;   // shared memory of one SM
 constexpr int SMEM_RESERVED = 1024;       // reserved by the system per CTA
 constexpr int MERGE_HEADS = 4;            // query heads merged per round
-constexpr int MERGE_STAGED_PARTS = 8;     // from this many partitions the final merge stages (M, L)
+constexpr int MERGE_BATCH = 16;           // partition records fetched together by a final merge
 
 // Softmax reference-max slack (log2 domain): P stays <= 2^8 and the rescale
 // of O is rare.
@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
     const bool abort = s_int[3] != 0;
 
     // ---- split-context completion: the CTA that wrote a sequence's last
-    // partition record merges all of them (one pass, running max) ----------
+    // partition record merges all of them ------------------------------------
     if (!abort && nparts > 1) {
       if (tid == 0) {
         __threadfence();   // release the records (ordered before by the barrier)
@@ -692,108 +692,57 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
       }
       __syncthreads();
       if (s_int[4]) {
-        constexpr int Q4 = D / 4;   // threads per head, 4 dims each
-        const int nrec = gcount * nparts;
-        if (nparts >= MERGE_STAGED_PARTS && 2 * nrec <= NW * MERGE_HEADS * D) {
-          // Many partitions: the (M, L) of every (head, partition) fetched at
-          // once into shared memory; one warp per head takes the maximum M and
-          // the weights e^(M_p - M) and the merged sum; then each thread sums
-          // its 4 dims of two heads over the partitions with a pass's record
-          // loads all in flight (the running-max form below chains them).
-          float *rm = mg_o;             // [gcount][nparts] maxima, then weights
-          float *rl = mg_o + nrec;      // [gcount][nparts] sums
-          float *ltot = mg_ml;          // [gcount] merged sums
-          for (int i = tid; i < nrec; i += NW * 32) {
-            const int g = i / nparts, q = i - g * nparts;
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) +
-                                     ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts + q);
-            rm[i] = ml.x;
-            rl[i] = ml.y;
-          }
-          __syncthreads();
-          for (int g = w; g < gcount; g += NW) {
-            float M = -INFINITY;
-            for (int q = lane; q < nparts; q += 32) M = fmaxf(M, rm[g * nparts + q]);
+        // Each thread takes 4 dims (a float4) of one head and combines that
+        // slice of all nparts records, MERGE_BATCH records at a time with
+        // every load of a batch in flight: the running sum is rescaled to
+        // each batch's maximum, so a merge costs ceil(nparts / MERGE_BATCH)
+        // round trips to L2 per slice.
+        constexpr int Q4 = D / 4;
+        for (int idx = tid; idx < gcount * Q4; idx += NW * 32) {
+          const int g = idx / Q4;
+          const int d4 = idx - g * Q4;
+          const size_t rec0 = ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts;
+          const float2 *mlp = reinterpret_cast<const float2 *>(p.part_ml) + rec0;
+          const float4 *op = reinterpret_cast<const float4 *>(p.part_o + rec0 * D) + d4;
+          float M = -INFINITY, Lt = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q0 = 0; q0 < nparts; q0 += MERGE_BATCH) {
+            float2 ml[MERGE_BATCH];
+            float4 ov[MERGE_BATCH];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, off));
-            float Lt = 0.f;
-            for (int q = lane; q < nparts; q += 32) {
-              const float f = fast_exp2(rm[g * nparts + q] - M);
-              rm[g * nparts + q] = f;
-              Lt += f * rl[g * nparts + q];
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Lt += __shfl_xor_sync(FULL_MASK, Lt, off);
-            if (lane == 0) ltot[g] = Lt;
-          }
-          __syncthreads();
-          for (int i0 = tid; i0 < gcount * Q4; i0 += 2 * NW * 32) {
-            const int i1 = i0 + NW * 32;
-            const bool two = i1 < gcount * Q4;
-            const int g0 = i0 / Q4, g1 = two ? i1 / Q4 : g0;
-            const int e0 = i0 - g0 * Q4, e1 = two ? i1 - g1 * Q4 : e0;
-            const float4 *o0 = reinterpret_cast<const float4 *>(p.part_o) +
-                               ((size_t)s * p.num_q_heads + hq0 + g0) * p.max_parts * Q4 + e0;
-            const float4 *o1 = reinterpret_cast<const float4 *>(p.part_o) +
-                               ((size_t)s * p.num_q_heads + hq0 + g1) * p.max_parts * Q4 + e1;
-            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll 8
-            for (int q = 0; q < nparts; ++q) {
-              const float4 v0 = __ldcg(o0 + (size_t)q * Q4);
-              const float f0 = rm[g0 * nparts + q];
-              a0.x += f0 * v0.x; a0.y += f0 * v0.y; a0.z += f0 * v0.z; a0.w += f0 * v0.w;
-              if (two) {
-                const float4 v1 = __ldcg(o1 + (size_t)q * Q4);
-                const float f1 = rm[g1 * nparts + q];
-                a1.x += f1 * v1.x; a1.y += f1 * v1.y; a1.z += f1 * v1.z; a1.w += f1 * v1.w;
+            for (int i = 0; i < MERGE_BATCH; ++i) {
+              if (q0 + i < nparts) {
+                ml[i] = __ldcg(mlp + q0 + i);
+                ov[i] = __ldcg(op + (size_t)(q0 + i) * Q4);
+              } else {
+                ml[i] = make_float2(-INFINITY, 0.f);
+                ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
               }
             }
-            const float inv0 = 1.f / ltot[g0];
-            const size_t ob0 = out_base + (size_t)g0 * D + 4 * e0;
-            store_out(p.out, ob0 + 0, p.out_dtype, a0.x * inv0);
-            store_out(p.out, ob0 + 1, p.out_dtype, a0.y * inv0);
-            store_out(p.out, ob0 + 2, p.out_dtype, a0.z * inv0);
-            store_out(p.out, ob0 + 3, p.out_dtype, a0.w * inv0);
-            if (two) {
-              const float inv1 = 1.f / ltot[g1];
-              const size_t ob1 = out_base + (size_t)g1 * D + 4 * e1;
-              store_out(p.out, ob1 + 0, p.out_dtype, a1.x * inv1);
-              store_out(p.out, ob1 + 1, p.out_dtype, a1.y * inv1);
-              store_out(p.out, ob1 + 2, p.out_dtype, a1.z * inv1);
-              store_out(p.out, ob1 + 3, p.out_dtype, a1.w * inv1);
+            float Mb = M;
+#pragma unroll
+            for (int i = 0; i < MERGE_BATCH; ++i) Mb = fmaxf(Mb, ml[i].x);
+            // exp2(-inf) = 0: the first batch, and padding entries, weigh nothing
+            const float a = fast_exp2(M - Mb);
+            acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+            Lt *= a;
+#pragma unroll
+            for (int i = 0; i < MERGE_BATCH; ++i) {
+              const float f = fast_exp2(ml[i].x - Mb);
+              acc.x += f * ov[i].x;
+              acc.y += f * ov[i].y;
+              acc.z += f * ov[i].z;
+              acc.w += f * ov[i].w;
+              Lt += f * ml[i].y;
             }
+            M = Mb;
           }
-          __syncthreads();   // merge slots free again
-        } else {
-          // (few partitions, or more records than shared memory holds: one
-          // pass, running max)
-          for (int idx = tid; idx < gcount * Q4; idx += NW * 32) {
-            const int g = idx / Q4;
-            const int d4 = idx - g * Q4;
-            const size_t rec0 = ((size_t)s * p.num_q_heads + hq0 + g) * p.max_parts;
-            float M = -INFINITY, Lt = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int q = 0; q < nparts; ++q) {
-              const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + rec0 + q);
-              const float4 ov =
-                  __ldcg(reinterpret_cast<const float4 *>(p.part_o + (rec0 + q) * D) + d4);
-              const float Mn = fmaxf(M, ml.x);
-              const float a = fast_exp2(M - Mn), f = fast_exp2(ml.x - Mn);
-              acc.x = acc.x * a + f * ov.x;
-              acc.y = acc.y * a + f * ov.y;
-              acc.z = acc.z * a + f * ov.z;
-              acc.w = acc.w * a + f * ov.w;
-              Lt = Lt * a + f * ml.y;
-              M = Mn;
-            }
-            const float inv = 1.f / Lt;
-            const size_t ob = out_base + (size_t)g * D + 4 * d4;
-            store_out(p.out, ob + 0, p.out_dtype, acc.x * inv);
-            store_out(p.out, ob + 1, p.out_dtype, acc.y * inv);
-            store_out(p.out, ob + 2, p.out_dtype, acc.z * inv);
-            store_out(p.out, ob + 3, p.out_dtype, acc.w * inv);
-          }
+          const float inv = 1.f / Lt;
+          const size_t ob = out_base + (size_t)g * D + 4 * d4;
+          store_out(p.out, ob + 0, p.out_dtype, acc.x * inv);
+          store_out(p.out, ob + 1, p.out_dtype, acc.y * inv);
+          store_out(p.out, ob + 2, p.out_dtype, acc.z * inv);
+          store_out(p.out, ob + 3, p.out_dtype, acc.w * inv);
         }
       }
     }
