@@ -684,11 +684,14 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
     // partition record merges all of them ------------------------------------
     if (!abort && nparts > 1) {
       if (tid == 0) {
-        __threadfence();   // release the records (ordered before by the barrier)
-        const bool last =
-            atomicAdd(p.seq_done + (size_t)s * HC + hc, 1u) == (unsigned)(nparts - 1);
-        if (last) __threadfence();
-        s_int[4] = last;
+        // release: the records (ordered before this by the barrier) are
+        // visible to whoever sees the count; acquire: the last one sees all
+        unsigned prev;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(p.seq_done + (size_t)s * HC + hc)
+                     : "memory");
+        s_int[4] = prev == (unsigned)(nparts - 1);
       }
       __syncthreads();
       if (s_int[4]) {
