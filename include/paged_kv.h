@@ -309,9 +309,9 @@ pkv_status paged_attention_chunked(
 /*
  * paged_attention_mixed -- paged_attention_chunked for a batch that mixes
  * decode tokens with prompt chunks, as continuous batching builds one step
- * ("Paging the KV Cache Like an OS", continuous batching: the scheduler puts
- * every waiting decode in the step before it fills the rest of the token
- * budget with prefill chunks).
+ * ("Paging the KV Cache Like an OS", continuous batching: a step takes all
+ * sequences that are decoding first and spends what is left of its token
+ * budget on pieces of prompts).
  *
  * Same arguments, layouts and result as paged_attention_chunked, plus the
  * decode attention's partition size and workspace.  A sequence with exactly
