@@ -120,10 +120,12 @@ pkv_status paged_kv_write(const void *key, const void *value, void *k_cache,
  *
  * Preconditions (the block manager's invariants): every dst appears once and
  * no dst is also a src in the same call.  The pairs live on the device, so
- * the kernel checks them: a pair whose dst is another pair's dst or src is
- * skipped and flagged (PKV_FLAG_PAIR_CONFLICT) -- the copies of one call run
- * in no particular order -- and a pair naming a block outside [0, num_blocks)
- * is skipped and flagged (PKV_FLAG_PAIR_RANGE).  num_pairs == 0 is a no-op.
+ * the kernel checks them: a pair naming a block outside [0, num_blocks) is
+ * skipped and flagged (PKV_FLAG_PAIR_RANGE) and copies nothing; a pair whose
+ * dst is another in-pool pair's dst or src is skipped and flagged
+ * (PKV_FLAG_PAIR_CONFLICT) -- the copies of one call run in no particular
+ * order.  A pair that copies a block onto itself conflicts only through other
+ * pairs.  num_pairs == 0 is a no-op.
  *
  * Cost of the check: each CTA compares its pair with every other pair
  * (O(num_pairs) reads per CTA, from L2), which is nothing for the few copies

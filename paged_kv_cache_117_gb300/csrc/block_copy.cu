@@ -80,7 +80,8 @@ __global__ void __launch_bounds__(COPY_THREADS)
   }
   // A pair whose dst is also another pair's dst or src would race: it is
   // skipped and flagged (the block manager never produces one).  A pair that
-  // copies a block onto itself clashes with no one.
+  // copies a block onto itself clashes with no one.  Pairs outside the pool
+  // copy nothing, so they clash with no one either (in both checks).
   bool clash = false;
   if (cnt != nullptr) {
     if (threadIdx.x == 0)
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(COPY_THREADS)
       if (i == pair) continue;
       const long long si = __ldg(reinterpret_cast<const long long *>(pairs) + 2 * i);
       const long long di = __ldg(reinterpret_cast<const long long *>(pairs) + 2 * i + 1);
-      clash |= si == dst || di == dst;
+      clash |= pair_in_range(si, di, num_blocks) && (si == dst || di == dst);
     }
   }
   if (__syncthreads_or(clash)) {
