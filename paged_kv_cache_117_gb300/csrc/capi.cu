@@ -261,7 +261,7 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
                        int block_size, int num_blocks, float scale, int partition_tokens,
                        void *workspace, size_t workspace_bytes, pkv_stream_t stream,
                        const char *what, const int32_t *query_start = nullptr,
-                       int num_tokens = 0) {
+                       int num_tokens = 0, int beside_chunked = 0) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks <= 0 || partition_tokens < 0)
     return PKV_ERR_RANGE;
@@ -362,6 +362,19 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
   p.v_pool = key_new ? v_cache : nullptr;
   p.query_start = query_start;
   p.num_tokens = num_tokens;
+  if (beside_chunked && query_start && group <= 8) {
+    // The SM split between this pass and the chunked pass beside it, from
+    // measurements of the two kernels on a 152-SM GB300: the decode pass
+    // streams 5.57 TB/s on 76 SMs, 6.30 on 114 and 6.52 on 152 (fitted by
+    // 7.87 TB/s * x / (x + 31.4)); the chunked pass's rate per SM, 6 TFLOP/s
+    // (995 TFLOP/s over 152 SMs on long chunks is 6.5), is the value a sweep
+    // on a 256-row + 8-chunk batch found best (5.4 and 6.0 alike; 4.8 and
+    // 6.8 slower).
+    p.overlap = 1;
+    p.ovl_peak_bps = 7.87e12;
+    p.ovl_half_sms = 31.4;
+    p.ovl_flops_sm = 6.0e12;
+  }
 
   int launches = 0;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -419,7 +432,7 @@ pkv_status chunked_impl(void *out, pkv_dtype out_dtype, const void *q, const voi
                         int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int num_blocks, float scale, pkv_p_format p_format,
                         pkv_stream_t stream, int skip_single, bool validate_only,
-                        const char *what) {
+                        const char *what, unsigned *ovl_done = nullptr) {
   if (p_format != PKV_P_HILO && p_format != PKV_P_F16) return PKV_ERR_DTYPE;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
@@ -502,6 +515,7 @@ pkv_status chunked_impl(void *out, pkv_dtype out_dtype, const void *q, const voi
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.flags = flags;
+  p.ovl_done = ovl_done;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e =
       dtype == PKV_BF16 ? pkv::launch_chunked_bf16(qmap, kmap, vmap, p, head_dim, block_size, st)
@@ -544,18 +558,27 @@ pkv_status paged_attention_mixed(void *out, pkv_dtype out_dtype, const void *q,
   if (st != PKV_OK || num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return st;
   if (num_seqs > 65535) return PKV_ERR_RANGE;
   if (!workspace) return PKV_ERR_WORKSPACE;
-  // the decode rows (sequences with one query row), then the chunks; the two
-  // kernels write disjoint rows of out and only read the pool
+  // The decode rows (sequences with one query row), then the chunks; the two
+  // kernels write disjoint rows of out and only read the pool.  With chunks
+  // in the batch and a group of at most 8 heads, the two passes run at the
+  // same time on disjoint SMs: the decode pass holds whole SMs (three
+  // decoders per CTA) and keeps the share its work list picks, the chunked
+  // pass takes the rest as they free up, and its grid ends after the decode
+  // grid (its finished-CTA counter is word 3 of the workspace's control
+  // block, zeroed by the decode work list).
+  const bool ovl = max_query_len >= 2 && num_q_heads / num_kv_heads <= 8;
   st = decode_impl(out, out_dtype, q, nullptr, nullptr, const_cast<void *>(k_cache),
                    const_cast<void *>(v_cache), dtype, block_tables, max_blocks, context_lens,
                    num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                    partition_tokens, workspace, workspace_bytes, stream,
-                   "paged_attention_mixed decode launch", query_start, num_tokens);
+                   "paged_attention_mixed decode launch", query_start, num_tokens, ovl ? 1 : 0);
   if (st != PKV_OK || max_query_len < 2) return st;
+  unsigned *ovl_done = ovl ? static_cast<unsigned *>(workspace) + 3 : nullptr;
   return chunked_impl(out, out_dtype, q, k_cache, v_cache, dtype, block_tables, max_blocks,
                       context_lens, query_start, num_seqs, num_tokens, max_query_len,
                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                      p_format, stream, 1, false, "paged_attention_mixed chunked launch");
+                      p_format, stream, 1, false, "paged_attention_mixed chunked launch",
+                      ovl_done);
 }
 
 pkv_status pkv_read_device_flags(uint32_t *flags_out, int clear, pkv_stream_t stream) {

@@ -194,7 +194,14 @@ __device__ __forceinline__ void store_row32(void *out, size_t base, int out_dtyp
   }
 }
 
-template <typename T, int D, int B, bool P16>
+// OVL: the chunked pass of a mixed batch whose decode pass (the kernel
+// before this one, launched first) still runs on other SMs.  The decode
+// grid lets this one start as soon as it holds its SMs, and everything this
+// kernel reads was complete before the decode grid started, so it does not
+// wait for its predecessor at the start; instead the last of its CTAs to
+// leave waits for the decode grid, so that this grid ends after it and the
+// stream's next work sees both passes done.
+template <typename T, int D, int B, bool P16, bool OVL>
 __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat16>::value), 1)
     chunked_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
@@ -221,7 +228,13 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   // adjacent in the grid, heaviest (last) pair first, so that they run at
   // the same time and read each K/V tile from L2 rather than from HBM.
   int s, kvh, pr_rev;
-  pdl_wait_predecessors();
+  // (OVL) every way out of the kernel passes here once per CTA
+  auto ovl_leave = [&]() {
+    if constexpr (OVL) {
+      if (tid == 0 && atomicAdd(p.ovl_done, 1u) == gridDim.x - 1) pdl_wait_predecessors();
+    }
+  };
+  if constexpr (!OVL) pdl_wait_predecessors();
   // Up to CK_ORDER_MAX sequences launch longest context first (ties by
   // index; more keep index order): the CTAs of the longest contexts start in
   // the first waves and the last wave holds short ones, so the SMs run out of
@@ -276,7 +289,10 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
     // (the grid is an upper bound; it falls short only when query ranges
     // overlap, which no valid batch has)
     if (b == 0 && tid == 0 && total > (int)gridDim.x) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
-    if (b >= total || r < 0) return;
+    if (b >= total || r < 0) {
+      ovl_leave();
+      return;
+    }
     s = ord_s[r];
     const int units = (r + 1 < S ? cnt_s[r + 1] : total) - cnt_s[r];
     const int npairs = units / p.num_kv_heads;
@@ -300,21 +316,31 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   fence_proxy_async_smem();   // the scratch is a TMA destination later
   const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
   const int n = q1 - q0;
-  if (p.skip_single && n == 1) return;   // a decode row: the decode kernel's
+  if (p.skip_single && n == 1) {   // a decode row: the decode kernel's
+    ovl_leave();
+    return;
+  }
   int L = p.context_lens[s];
   if (q0 < 0 || n < 0 || q1 > p.num_tokens || n > p.max_query_len || L < n) {
     if (tid == 0 && pr_rev == 0 && kvh == 0) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
+    ovl_leave();
     return;
   }
   if (L > p.max_blocks * B) {
     if (tid == 0 && pr_rev == 0 && kvh == 0) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
     L = p.max_blocks * B;
-    if (L < n) return;
+    if (L < n) {
+      ovl_leave();
+      return;
+    }
   }
   const int TQ = p.tile_tokens;
   const int G = p.group;
   const int nq = (n + TQ - 1) / TQ;
-  if (2 * pr_rev >= nq) return;
+  if (2 * pr_rev >= nq) {
+    ovl_leave();
+    return;
+  }
   int tb[2], te[2], pm[2], nk[2];              // per query tile: tokens [tb, te), last
   tb[0] = (nq - 1 - 2 * pr_rev) * TQ;          // position, KV tiles it needs
   tb[1] = tb[0] - TQ;                          // tile B: the TQ tokens before A's
@@ -329,6 +355,7 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
 
   if (sb & 1023u) {   // the swizzled tiles need a 1 KiB-aligned base
     if (tid == 0) atomicOr(p.flags, PKV_FLAG_TIMEOUT);
+    ovl_leave();
     return;
   }
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C::OFF_TMEM);
@@ -878,17 +905,18 @@ __global__ void __launch_bounds__(ck_threads(P16 && std::is_same<T, __nv_bfloat1
   tc::fence_before_sync();
   __syncthreads();
   if (warp == CK_MMA) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  ovl_leave();
   pdl_launch_dependents();
 }
 
 // ---- host side ---------------------------------------------------------------
 
-template <typename T, int D, int B, bool P16>
+template <typename T, int D, int B, bool P16, bool OVL>
 cudaError_t launch_chunked_p(const CUtensorMap &qmap, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, const ChunkedParams &p,
                              cudaStream_t stream) {
   using C = ChunkCfg<D>;
-  auto kern = chunked_kernel<T, D, B, P16>;
+  auto kern = chunked_kernel<T, D, B, P16, OVL>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -914,8 +942,13 @@ template <typename T, int D, int B>
 cudaError_t launch_chunked_cfg(const CUtensorMap &qmap, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, const ChunkedParams &p,
                                cudaStream_t stream) {
-  return p.p_format == PKV_P_F16 ? launch_chunked_p<T, D, B, true>(qmap, kmap, vmap, p, stream)
-                                 : launch_chunked_p<T, D, B, false>(qmap, kmap, vmap, p, stream);
+  if (p.ovl_done)   // beside a running decode pass (mixed batch)
+    return p.p_format == PKV_P_F16
+               ? launch_chunked_p<T, D, B, true, true>(qmap, kmap, vmap, p, stream)
+               : launch_chunked_p<T, D, B, false, true>(qmap, kmap, vmap, p, stream);
+  return p.p_format == PKV_P_F16
+             ? launch_chunked_p<T, D, B, true, false>(qmap, kmap, vmap, p, stream)
+             : launch_chunked_p<T, D, B, false, false>(qmap, kmap, vmap, p, stream);
 }
 
 template <typename T, int D>

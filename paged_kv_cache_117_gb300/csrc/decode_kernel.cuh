@@ -113,6 +113,10 @@ struct DecodeCfg {
   static constexpr int STAGES_BYTES = round_up_c(NW * STAGES * STAGE_BYTES, 1024);
   static constexpr int MERGE_FLOATS = NW * MERGE_HEADS * (D + 2);
   static constexpr int SMEM_BYTES = smem_bytes_c<D>(STAGES);
+  // Grouped form (WG groups of NW warps in one CTA, each an independent
+  // decoder with its own shared memory): the groups' regions, 1 KiB apart.
+  static constexpr int GROUP_STRIDE = round_up_c(SMEM_BYTES - 1024, 1024);
+  static constexpr int smem_for(int wg) { return wg == 1 ? SMEM_BYTES : 1024 + wg * GROUP_STRIDE; }
 
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(B == 4 || B == 8 || B == 16 || B == 32, "block_size");
@@ -174,7 +178,14 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   slot[tid] = 0;
   __syncthreads();
   int nf = 0;
+  double dec_tok = 0.0, ch_pairs = 0.0;   // (overlap) decode tokens, visible query-key pairs
   for (int s = s0; s < s1; ++s) {
+    if (p.overlap) {
+      const int a = __ldg(p.query_start + s), n = __ldg(p.query_start + s + 1) - a;
+      const int Lc = clamp_len(__ldg(p.context_lens + s), cap);
+      if (n == 1) dec_tok += Lc;
+      else if (n >= 2 && Lc >= n) ch_pairs += (double)n * (Lc - n + 1) + 0.5 * (double)n * (n - 1);
+    }
     if (!mine(s, true)) continue;
     const int L0 = __ldg(p.context_lens + s);
     if (L0 < 0 || L0 > cap) atomicOr(p.flags, PKV_FLAG_LEN_RANGE);
@@ -226,11 +237,47 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
     }
   }
   for (int i = tid; i < S * p.num_hc; i += 1024) p.seq_done[i] = 0u;
+  unsigned active = (unsigned)p.grid;
+  if (p.overlap) {
+    // The decode pass's share of the SMs when the chunked pass runs beside
+    // it: x SMs stream the decode rows' K and V (bandwidth modelled as
+    // peak * x / (x + half), which saturates), the other M - x run the
+    // chunks' tensor work at a fixed rate per SM; x solves
+    // bytes (x + half) / (peak x) = flops / ((M - x) rate).
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      dec_tok += __shfl_xor_sync(FULL_MASK, dec_tok, off);
+      ch_pairs += __shfl_xor_sync(FULL_MASK, ch_pairs, off);
+    }
+    __shared__ double red[2][32];
+    if (lane == 0) { red[0][wid] = dec_tok; red[1][wid] = ch_pairs; }
+    __syncthreads();
+    if (tid == 0) {
+      double dt = 0.0, cp = 0.0;
+      for (int i = 0; i < 32; ++i) { dt += red[0][i]; cp += red[1][i]; }
+      const double A = dt * p.num_kv_heads * p.head_dim * 4.0 / p.ovl_peak_bps;   // K + V, 2 B
+      const double F = cp * p.num_q_heads * p.head_dim * 4.0 / p.ovl_flops_sm;
+      const double M = p.ovl_sms, h = p.ovl_half_sms;
+      double x = M;
+      if (A <= 0.0) x = 0.0;
+      else if (F > 0.0) {
+        const double bq = A * M - A * h - F;
+        x = (bq + sqrt(bq * bq + 4.0 * A * A * h * M)) / (2.0 * A);
+      }
+      const int gcta = p.grid / p.ovl_wg;   // decode CTAs launched
+      int xi = (int)ceil(x);
+      xi = xi < 0 ? 0 : (xi > gcta ? gcta : xi);
+      if (A > 0.0 && xi == 0) xi = 1;
+      active = (unsigned)(xi * p.ovl_wg);
+    }
+  }
   if (tid == 0) {
-    // CTA c of the attention grid starts with units c and c + grid without
-    // asking; the counter hands out the rest
-    p.ctrl[0] = 2u * (unsigned)p.grid;
+    // CTA c of the attention grid starts with units c and c + (CTAs running)
+    // without asking; the counter hands out the rest
+    p.ctrl[0] = 2u * active;
     p.ctrl[1] = (unsigned)(total_f + total_p) * (unsigned)p.num_hc;
+    p.ctrl[2] = active;   // decoders that run (all, unless a chunked pass runs beside)
+    p.ctrl[3] = 0u;       // chunked CTAs finished (when it does)
   }
 }
 
@@ -310,16 +357,30 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qb)[D / 16][NH][2], cons
 }
 
 // ---------------------------------------------------------------------------
-template <typename T, int D, int B, int NH>
-__global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
+// WG = 1: one decoder per CTA (several CTAs per SM).  WG = 3: three
+// decoders of NW warps each in one CTA that takes a whole SM -- the form a
+// mixed batch uses, so that the decode pass holds whole SMs and the chunked
+// pass can run on the others at the same time.  Each group works exactly as
+// a CTA of the WG = 1 form (own shared memory, own barrier, own units); only
+// the group-wide barrier and the virtual CTA index differ.
+template <typename T, int D, int B, int NH, int WG>
+__global__ void __launch_bounds__(DECODE_WARPS * 32 * WG, WG == 1 ? occupancy_c<D, NH>() : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using C = DecodeCfg<T, D, B, NH>;
   constexpr int NW = C::NW;
   constexpr int STAGES = C::STAGES;
+  static_assert(WG == 1 || (NH == 1 && C::OCC == 3), "grouped form: one 8-head tile, 3 per SM");
   extern __shared__ unsigned char smem_raw[];
+  const int wg = WG == 1 ? 0 : (int)(threadIdx.x / (NW * 32));
   unsigned char *smem = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) + wg * C::GROUP_STRIDE;
+  // the group's barrier: the whole CTA in the WG = 1 form, else named
+  // barrier 1 + wg over the group's NW warps
+  auto group_sync = [&]() {
+    if (WG == 1) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"r"(1 + wg), "r"(NW * 32) : "memory");
+  };
   const uint32_t stage_smem = smem_addr(smem);
   float *mg_o = reinterpret_cast<float *>(smem + C::STAGES_BYTES);      // [NW][4][D]
   float *mg_ml = mg_o + NW * MERGE_HEADS * D;                          // [NW][4][2]
@@ -327,7 +388,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   // s_int[0..2]: ring of upcoming unit ids, s_int[3]: abort, s_int[4]: last
   volatile int *s_int = reinterpret_cast<volatile int *>(bars + NW * STAGES);
 
-  const int tid = threadIdx.x;
+  const int tid = (int)threadIdx.x - wg * NW * 32;   // thread within the group
   const int lane = tid & 31, w = tid >> 5;
   const int HC = p.num_hc;
 
@@ -350,16 +411,27 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   // everything above is local; the work list, the pool and q come from the
   // kernels before this one
   pdl_wait_predecessors();
+  // Decoders (groups) of the grid: vb is this one's index.  The grouped form
+  // runs only the first ctrl[2] of them (the work list's share of the SMs):
+  // it lets the next kernel on the stream start now, and a CTA with no
+  // running group leaves at once so that its SM goes to that kernel.
+  const unsigned vb = blockIdx.x * WG + wg;
+  unsigned vgrid = gridDim.x * WG;
+  if (WG > 1) {
+    vgrid = __ldcg(p.ctrl + 2);
+    pdl_launch_dependents();
+    if (blockIdx.x * WG >= vgrid) return;
+  }
   // The first two units need no atomic (the counter starts past them), and
   // their work-list entries are fetched together with the unit count (an
   // entry past the list is read, from inside the array, but never used).
-  unsigned cur_unit = blockIdx.x;
-  unsigned nxt_unit = blockIdx.x + gridDim.x;
+  unsigned cur_unit = vb < vgrid ? vb : 0xFFFFFFFFu;
+  unsigned nxt_unit = vb < vgrid ? vb + vgrid : 0xFFFFFFFFu;
   const size_t last_item = (size_t)p.num_seqs * p.max_parts - 1;
   const int2 item0 = __ldcg(p.items + min((size_t)(cur_unit / HC), last_item));
   const int2 item1 = __ldcg(p.items + min((size_t)(nxt_unit / HC), last_item));
   const unsigned total = __ldcg(p.ctrl + 1);
-  __syncthreads();
+  group_sync();
 
   const uint32_t wst = stage_smem + w * STAGES * C::STAGE_BYTES;
   const uint32_t bar0 = smem_addr(bars + w * STAGES);
@@ -648,7 +720,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
             }
           }
         }
-      __syncthreads();
+      group_sync();
       if (s_int[3] == 0) {
         for (int idx = tid; idx < hn * D; idx += NW * 32) {
           const int g = idx / D;
@@ -676,7 +748,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
           }
         }
       }
-      __syncthreads();   // merge slots free again; this round's records written
+      group_sync();   // merge slots free again; this round's records written
     }
     const bool abort = s_int[3] != 0;
 
@@ -693,7 +765,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
                      : "memory");
         s_int[4] = prev == (unsigned)(nparts - 1);
       }
-      __syncthreads();
+      group_sync();
       if (s_int[4]) {
         // Each thread takes 4 dims (a float4) of one head and combines that
         // slice of all nparts records, MERGE_BATCH records at a time with
@@ -773,7 +845,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, occupancy_c<D, NH>())
   // never leave with copies in flight into this CTA's shared memory
   for (; use_cnt < ld_cnt; ++use_cnt)
     (void)mbar_wait_bounded(bar0 + (use_cnt % STAGES) * 8, (use_cnt / STAGES) & 1u);
-  pdl_launch_dependents();
+  if (WG == 1) pdl_launch_dependents();
 }
 
 // ---- host-side launch -------------------------------------------------------
@@ -814,29 +886,31 @@ cudaError_t launch_info(const void *fn, int threads, int smem, int dev, LaunchIn
 }
 }  // namespace
 
-template <typename T, int D, int B, int NH>
+template <typename T, int D, int B, int NH, int WG>
 cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeParams &p, cudaStream_t stream, int *launches) {
   using C = DecodeCfg<T, D, B, NH>;
-  auto kern = decode_kernel<T, D, B, NH>;
+  auto kern = decode_kernel<T, D, B, NH, WG>;
+  constexpr int smem = C::smem_for(WG);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   LaunchInfo li;
-  e = launch_info(reinterpret_cast<const void *>(kern), C::NW * 32, C::SMEM_BYTES, dev, &li);
+  e = launch_info(reinterpret_cast<const void *>(kern), C::NW * 32 * WG, smem, dev, &li);
   if (e != cudaSuccess) return e;
   const long long units_max =
       (long long)p.num_seqs * p.max_parts * p.num_hc;   // upper bound on work units
-  long long grid = (long long)li.sms * li.ctas_per_sm;
-  if (grid > units_max) grid = units_max;
+  long long grid = (long long)li.sms * li.ctas_per_sm;   // CTAs
+  if (grid * WG > units_max) grid = (units_max + WG - 1) / WG;
   if (grid < 1) grid = 1;
   DecodeParams pg = p;
-  pg.grid = (int)grid;
+  pg.grid = (int)grid * WG;   // decoders
+  pg.ovl_wg = WG;
+  pg.ovl_sms = li.sms;
   e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, stream, pg);
   if (e != cudaSuccess) return e;
   ++*launches;
-  e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::NW * 32), C::SMEM_BYTES, stream, kmap, vmap,
-                 pg);
+  e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::NW * 32 * WG), smem, stream, kmap, vmap, pg);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaSuccess;
@@ -845,8 +919,12 @@ cudaError_t launch_decode_cfg(const CUtensorMap &kmap, const CUtensorMap &vmap,
 template <typename T, int D, int B>
 cudaError_t launch_decode_nh(const CUtensorMap &kmap, const CUtensorMap &vmap,
                              const DecodeParams &p, cudaStream_t stream, int *launches) {
-  if (p.group <= 8) return launch_decode_cfg<T, D, B, 1>(kmap, vmap, p, stream, launches);
-  return launch_decode_cfg<T, D, B, 2>(kmap, vmap, p, stream, launches);
+  if (p.group <= 8) {
+    // a mixed batch whose chunked pass runs beside: the grouped form
+    if (p.overlap) return launch_decode_cfg<T, D, B, 1, 3>(kmap, vmap, p, stream, launches);
+    return launch_decode_cfg<T, D, B, 1, 1>(kmap, vmap, p, stream, launches);
+  }
+  return launch_decode_cfg<T, D, B, 2, 1>(kmap, vmap, p, stream, launches);
 }
 
 template <typename T, int D>

@@ -62,7 +62,8 @@ struct DecodeParams {
   int max_parts;                 // partitions per sequence the workspace holds
   float *part_ml;                // [S, Hq, max_parts, 2]  (running max, sum)
   float *part_o;                 // [S, Hq, max_parts, D]  unnormalised output
-  unsigned *ctrl;                // [0] next work unit, [1] number of work units
+  unsigned *ctrl;                // [0] next work unit, [1] number of work units,
+                                 // [2] decoders that run, [3] chunked CTAs finished
   int grid = 0;                  // CTAs of the attention grid (set at launch)
   unsigned *seq_done;            // [S, num_hc] partitions finished per sequence
   int2 *items;                   // [S * max_parts] (sequence, partition) work list
@@ -79,6 +80,16 @@ struct DecodeParams {
   // the chunked kernel).
   const int32_t *query_start = nullptr;
   int num_tokens = 0;            // rows of q and out when query_start is set
+  // A mixed batch whose chunked pass runs at the same time as this decode
+  // pass (overlap = 1, group <= 8): the work list picks how many SMs the
+  // decode pass keeps (ctrl[2] decoders) from this model of the two passes,
+  // and the decode CTAs hold whole SMs, ovl_wg decoders each.
+  int overlap = 0;
+  int ovl_wg = 1;                // decoders per CTA (set at launch)
+  int ovl_sms = 0;               // SMs of the device (set at launch)
+  double ovl_peak_bps = 0.0;     // decode bandwidth model: peak * x / (x + half) on x SMs
+  double ovl_half_sms = 0.0;
+  double ovl_flops_sm = 0.0;     // chunked pass: flop/s per SM
 };
 
 // Launch the work-list pass and the decode pass for one cache dtype /
@@ -114,6 +125,10 @@ struct ChunkedParams {
   int num_blocks;
   float scale_log2;
   unsigned *flags;
+  // Non-null: the chunked pass of a mixed batch that runs beside the decode
+  // pass launched just before it; counts this grid's finished CTAs (zeroed
+  // by the decode work list), and the last one waits for the decode grid.
+  unsigned *ovl_done = nullptr;
 };
 
 cudaError_t launch_chunked_bf16(const CUtensorMap &qmap, const CUtensorMap &kmap,
