@@ -333,10 +333,18 @@ pkv_status paged_attention_chunked(
  *                     bytes, 256-byte aligned, no initial contents needed;
  *                     calls that share one must not overlap in time.
  *
- * Two or three kernels in stream order (the decode work list, the decode
- * pass, then the chunked pass when max_query_len > 1); they write disjoint
- * rows of out.  Every argument is checked before the first launch; errors as
- * paged_attention_chunked and paged_attention_decode.  A single-row sequence
+ * Two or three kernels (the decode work list, the decode pass, then the
+ * chunked pass when max_query_len > 1); they write disjoint rows of out.
+ * With max_query_len > 1 and at most 8 query heads per KV head the two
+ * passes run at the same time on disjoint SMs: the work list gives the
+ * decode pass the share of the SMs that a model of the two passes (its K/V
+ * bytes against the chunks' query-key pairs) says balances them, and the
+ * chunked pass starts on the rest at once.  The call still behaves as stream
+ * ordered: the chunked grid ends only after the decode grid, so work queued
+ * behind the call on `stream` sees out complete.  (The workspace's first
+ * bytes carry the split and a finished-CTA count for this.)  Every argument
+ * is checked before the first launch; errors as paged_attention_chunked and
+ * paged_attention_decode.  A single-row sequence
  * whose row lies outside [0, num_tokens) or whose context length is below 1
  * is skipped and flagged (PKV_FLAG_LEN_RANGE).
  */

@@ -364,16 +364,18 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
   p.num_tokens = num_tokens;
   if (beside_chunked && query_start && group <= 8) {
     // The SM split between this pass and the chunked pass beside it, from
-    // measurements of the two kernels on a 152-SM GB300: the decode pass
-    // streams 5.57 TB/s on 76 SMs, 6.30 on 114 and 6.52 on 152 (fitted by
-    // 7.87 TB/s * x / (x + 31.4)); the chunked pass's rate per SM, 6 TFLOP/s
-    // (995 TFLOP/s over 152 SMs on long chunks is 6.5), is the value a sweep
-    // on a 256-row + 8-chunk batch found best (5.4 and 6.0 alike; 4.8 and
-    // 6.8 slower).
+    // measurements of the two kernels on a 152-SM GB300.  The decode pass
+    // in its grouped form, confined to x SMs, streams 5.00, 5.61, 5.94, 6.25
+    // and 6.39 TB/s on 76, 100, 120, 136 and 152 SMs: 9.15 TB/s * x / (x +
+    // 63) within 1.5 %.  The chunked pass's rate per SM, 5.5 TFLOP/s, lies
+    // between its rate on these chunks run alone (4.8: waves of a 512-CTA
+    // grid) and on long chunks (6.5); it is the value at which the split
+    // lands where sweeps of a 256-row + 8-chunk batch found the call
+    // fastest (~75 of 152 SMs for the decode rows; 66, 70 and 80+ slower).
     p.overlap = 1;
-    p.ovl_peak_bps = 7.87e12;
-    p.ovl_half_sms = 31.4;
-    p.ovl_flops_sm = 6.0e12;
+    p.ovl_peak_bps = 9.15e12f;
+    p.ovl_half_sms = 63.f;
+    p.ovl_flops_sm = 5.5e12f;
   }
 
   int launches = 0;

@@ -178,13 +178,15 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   slot[tid] = 0;
   __syncthreads();
   int nf = 0;
-  double dec_tok = 0.0, ch_pairs = 0.0;   // (overlap) decode tokens, visible query-key pairs
+  // (overlap) decode tokens and visible (query, key) pairs of the chunks, exact
+  long long dec_tok = 0, ch_pairs = 0;
   for (int s = s0; s < s1; ++s) {
     if (p.overlap) {
       const int a = __ldg(p.query_start + s), n = __ldg(p.query_start + s + 1) - a;
       const int Lc = clamp_len(__ldg(p.context_lens + s), cap);
       if (n == 1) dec_tok += Lc;
-      else if (n >= 2 && Lc >= n) ch_pairs += (double)n * (Lc - n + 1) + 0.5 * (double)n * (n - 1);
+      else if (n >= 2 && Lc >= n)
+        ch_pairs += (long long)n * (Lc - n + 1) + (long long)n * (n - 1) / 2;
     }
     if (!mine(s, true)) continue;
     const int L0 = __ldg(p.context_lens + s);
@@ -249,23 +251,32 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
       dec_tok += __shfl_xor_sync(FULL_MASK, dec_tok, off);
       ch_pairs += __shfl_xor_sync(FULL_MASK, ch_pairs, off);
     }
-    __shared__ double red[2][32];
+    __shared__ long long red[2][32];
     if (lane == 0) { red[0][wid] = dec_tok; red[1][wid] = ch_pairs; }
     __syncthreads();
+    if (wid == 0) {
+      long long dt = red[0][lane], cp = red[1][lane];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        dt += __shfl_xor_sync(FULL_MASK, dt, off);
+        cp += __shfl_xor_sync(FULL_MASK, cp, off);
+      }
+      dec_tok = dt;
+      ch_pairs = cp;
+    }
     if (tid == 0) {
-      double dt = 0.0, cp = 0.0;
-      for (int i = 0; i < 32; ++i) { dt += red[0][i]; cp += red[1][i]; }
-      const double A = dt * p.num_kv_heads * p.head_dim * 4.0 / p.ovl_peak_bps;   // K + V, 2 B
-      const double F = cp * p.num_q_heads * p.head_dim * 4.0 / p.ovl_flops_sm;
-      const double M = p.ovl_sms, h = p.ovl_half_sms;
-      double x = M;
-      if (A <= 0.0) x = 0.0;
-      else if (F > 0.0) {
-        const double bq = A * M - A * h - F;
-        x = (bq + sqrt(bq * bq + 4.0 * A * A * h * M)) / (2.0 * A);
+      // in seconds x SMs (single precision: a few digits decide an SM count)
+      const float A = (float)dec_tok * (float)(p.num_kv_heads * p.head_dim * 4) / p.ovl_peak_bps;
+      const float F = (float)ch_pairs * (float)(p.num_q_heads * p.head_dim * 4) / p.ovl_flops_sm;
+      const float M = (float)p.ovl_sms, h = p.ovl_half_sms;
+      float x = M;
+      if (A <= 0.f) x = 0.f;
+      else if (F > 0.f) {
+        const float bq = A * M - A * h - F;
+        x = (bq + sqrtf(bq * bq + 4.f * A * A * h * M)) / (2.f * A);
       }
       const int gcta = p.grid / p.ovl_wg;   // decode CTAs launched
-      int xi = (int)ceil(x);
+      int xi = (int)ceilf(x);
       xi = xi < 0 ? 0 : (xi > gcta ? gcta : xi);
       if (A > 0.0 && xi == 0) xi = 1;
       active = (unsigned)(xi * p.ovl_wg);

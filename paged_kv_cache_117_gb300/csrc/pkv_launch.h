@@ -87,9 +87,9 @@ struct DecodeParams {
   int overlap = 0;
   int ovl_wg = 1;                // decoders per CTA (set at launch)
   int ovl_sms = 0;               // SMs of the device (set at launch)
-  double ovl_peak_bps = 0.0;     // decode bandwidth model: peak * x / (x + half) on x SMs
-  double ovl_half_sms = 0.0;
-  double ovl_flops_sm = 0.0;     // chunked pass: flop/s per SM
+  float ovl_peak_bps = 0.f;      // decode bandwidth model: peak * x / (x + half) on x SMs
+  float ovl_half_sms = 0.f;
+  float ovl_flops_sm = 0.f;      // chunked pass: flop/s per SM
 };
 
 // Launch the work-list pass and the decode pass for one cache dtype /
