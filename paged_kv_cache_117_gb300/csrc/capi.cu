@@ -575,7 +575,11 @@ pkv_status paged_attention_mixed(void *out, pkv_dtype out_dtype, const void *q,
                    partition_tokens, workspace, workspace_bytes, stream,
                    "paged_attention_mixed decode launch", query_start, num_tokens, ovl ? 1 : 0);
   if (st != PKV_OK || max_query_len < 2) return st;
-  unsigned *ovl_done = ovl ? static_cast<unsigned *>(workspace) + 3 : nullptr;
+  unsigned *ovl_done =
+      ovl ? reinterpret_cast<unsigned *>(static_cast<unsigned char *>(workspace) +
+                                         pkv::WS_CTRL_OFFSET) +
+                pkv::WS_CTRL_CHUNKED_DONE
+          : nullptr;
   return chunked_impl(out, out_dtype, q, k_cache, v_cache, dtype, block_tables, max_blocks,
                       context_lens, query_start, num_seqs, num_tokens, max_query_len,
                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,

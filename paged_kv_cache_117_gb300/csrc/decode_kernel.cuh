@@ -288,7 +288,7 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
     p.ctrl[0] = 2u * active;
     p.ctrl[1] = (unsigned)(total_f + total_p) * (unsigned)p.num_hc;
     p.ctrl[2] = active;   // decoders that run (all, unless a chunked pass runs beside)
-    p.ctrl[3] = 0u;       // chunked CTAs finished (when it does)
+    p.ctrl[WS_CTRL_CHUNKED_DONE] = 0u;   // chunked CTAs finished (when it does)
   }
 }
 

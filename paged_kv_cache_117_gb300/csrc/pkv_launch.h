@@ -20,6 +20,11 @@ struct WorkspaceLayout {
 
 inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
+// The control block (64 uint32 words) opens the workspace: [0] next work
+// unit, [1] number of units, [2] decoders that run, [3] chunked CTAs finished.
+constexpr size_t WS_CTRL_OFFSET = 0;
+constexpr int WS_CTRL_CHUNKED_DONE = 3;
+
 inline WorkspaceLayout workspace_layout(long long S, long long Hq, long long D,
                                         long long max_context, long long partition_tokens) {
   WorkspaceLayout w{};
@@ -27,8 +32,8 @@ inline WorkspaceLayout workspace_layout(long long S, long long Hq, long long D,
   if (partition_tokens > 0) parts = (max_context + partition_tokens - 1) / partition_tokens;
   if (parts < 1) parts = 1;
   w.max_parts = (int)parts;
-  w.ctrl = 0;
-  w.seq_done = 256;
+  w.ctrl = WS_CTRL_OFFSET;
+  w.seq_done = WS_CTRL_OFFSET + 256;
   w.items = w.seq_done + round256((size_t)(S * Hq) * 4);
   w.part_o = w.items + round256((size_t)(S * parts) * 8);
   if (parts > 1) {
