@@ -1187,6 +1187,13 @@ def run_native_chunked(a, world, rank, local):
             "traffic": measured_traffic(w.name, 0, "chunked_kernel_prefill.md", CHUNKED_SOURCES)}
     extra = {}
     if mixed:
+        # the share of the SMs the work list gave the decode rows in the last
+        # call (word 2 of the workspace's control block: decoders that ran,
+        # three to an SM when the passes run side by side)
+        torch.cuda.synchronize()
+        ctrl = ws[:16].view(torch.int32).cpu().tolist()
+        side_by_side = w.num_q_heads // w.num_kv_heads <= 8 and maxq >= 2
+        decode_sms = ctrl[2] // 3 if side_by_side else None
         # the same batch in one paged_attention_chunked launch, for comparison
         sev = [(ev(), ev()) for _ in range(K)]
         host_head_start()
@@ -1212,7 +1219,9 @@ def run_native_chunked(a, world, rank, local):
                              f"{dec_bytes} B at the {hkind} {hbm} GB/s + chunks' {ch_flops} "
                              f"FLOP at the {kind} {peak} TFLOP/s", "unit": "floor / time",
                 "frac": round(floor_ms / dec_ms, 4), "traffic": None}
-        extra = {"single_chunked_call_ms": round(single_ms, 4),
+        extra = {"decode_sms": decode_sms,
+                 "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
+                 "single_chunked_call_ms": round(single_ms, 4),
                  "speedup_vs_single_chunked_call": round(single_ms / dec_ms, 3),
                  "decode_rows": n_dec, "decode_bytes": dec_bytes, "chunk_flops": ch_flops}
     return {

@@ -365,8 +365,10 @@ def paged_attention_mixed(out, q, k_cache, v_cache, block_tables, context_lens, 
                           workspace=None, stream=None):
     """paged_attention_chunked for a batch that mixes decode tokens with
     prompt chunks: the sequences with one query row run on the decode kernel
-    (rows found through query_start), the others on the tensor-core kernel.
-    A workspace tensor is allocated by torch when none is given."""
+    (rows found through query_start), the others on the tensor-core kernel;
+    with at most 8 query heads per KV head the two run side by side on
+    disjoint SMs.  A workspace tensor is allocated by torch when none is
+    given."""
     _need_cuda("paged_attention_mixed", out, q, k_cache, v_cache, block_tables, context_lens,
                query_start)
     N, B, Hkv, D = _cache_dims(k_cache)
