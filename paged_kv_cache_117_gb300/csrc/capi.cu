@@ -365,17 +365,23 @@ pkv_status decode_impl(void *out, pkv_dtype out_dtype, const void *q, const void
   if (beside_chunked && query_start && group <= 8) {
     // The SM split between this pass and the chunked pass beside it, from
     // measurements of the two kernels on a 152-SM GB300.  The decode pass
-    // in its grouped form, confined to x SMs, streams 5.00, 5.61, 5.94, 6.25
-    // and 6.39 TB/s on 76, 100, 120, 136 and 152 SMs: 9.15 TB/s * x / (x +
-    // 63) within 1.5 %.  The chunked pass's rate per SM, 5.5 TFLOP/s, lies
-    // between its rate on these chunks run alone (4.8: waves of a 512-CTA
-    // grid) and on long chunks (6.5); it is the value at which the split
-    // lands where sweeps of a 256-row + 8-chunk batch found the call
-    // fastest (~75 of 152 SMs for the decode rows; 66, 70 and 80+ slower).
+    // in its grouped form, confined to x SMs of the Llama-shaped batch,
+    // streams 71.5-73.2 GB/s per SM up to 56 SMs (0.88 TB/s on 12, 4.01 on
+    // 56), then 5.00, 5.61, 5.94, 6.25 and 6.39 TB/s on 76, 100, 120, 136 and
+    // 152: min(73 GB/s * x, 9.15 TB/s * x / (x + 63)) within 3 %.  The
+    // chunked pass's rate per SM, 5.5 TFLOP/s, lies between its rate on
+    // 512-token chunks run alone (4.8: waves of a 512-CTA grid) and on long
+    // chunks (6.5); it is the value at which the split lands where sweeps of
+    // a 256-row + 8-chunk batch found the call fastest (~75 of 152 SMs for
+    // the decode rows; 66, 70 and 80+ slower).  Side by side only when the
+    // model puts it 5 % ahead of the passes in turn: at the extremes (few
+    // decode SMs) it is least accurate.
     p.overlap = 1;
+    p.ovl_sm_bps = 73e9f;
     p.ovl_peak_bps = 9.15e12f;
     p.ovl_half_sms = 63.f;
     p.ovl_flops_sm = 5.5e12f;
+    p.ovl_margin = 0.05f;
   }
 
   int launches = 0;

@@ -242,43 +242,54 @@ static __global__ void __launch_bounds__(1024, 1) decode_plan_kernel(const Decod
   unsigned active = (unsigned)p.grid;
   if (p.overlap) {
     // The decode pass's share of the SMs when the chunked pass runs beside
-    // it: x SMs stream the decode rows' K and V (bandwidth modelled as
-    // peak * x / (x + half), which saturates), the other M - x run the
-    // chunks' tensor work at a fixed rate per SM; x solves
-    // bytes (x + half) / (peak x) = flops / ((M - x) rate).
+    // it.  With x SMs the decode rows' K/V stream at
+    //   bw(x) = min(per_sm * x, peak * x / (x + half))
+    // (linear while each SM's own rate binds, then saturating), and the
+    // chunks' query-key pairs run at a fixed tensor rate on the other M - x.
+    // Every x in [1, M) is tried (one thread each) for the smallest
+    // max(decode time, chunked time); unless that beats running the passes
+    // in turn by ovl_margin, the decode pass takes every SM (and the chunked
+    // CTAs follow as its CTAs leave).
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       dec_tok += __shfl_xor_sync(FULL_MASK, dec_tok, off);
       ch_pairs += __shfl_xor_sync(FULL_MASK, ch_pairs, off);
     }
     __shared__ long long red[2][32];
+    __shared__ unsigned long long best[32];
     if (lane == 0) { red[0][wid] = dec_tok; red[1][wid] = ch_pairs; }
     __syncthreads();
-    if (wid == 0) {
-      long long dt = red[0][lane], cp = red[1][lane];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        dt += __shfl_xor_sync(FULL_MASK, dt, off);
-        cp += __shfl_xor_sync(FULL_MASK, cp, off);
-      }
-      dec_tok = dt;
-      ch_pairs = cp;
+    long long dt = 0, cp = 0;
+    for (int i = 0; i < 32; ++i) { dt += red[0][i]; cp += red[1][i]; }   // every thread
+    const float bytes = (float)dt * (float)(p.num_kv_heads * p.head_dim * 4);   // K + V, 2 B
+    const float flops = (float)cp * (float)(p.num_q_heads * p.head_dim * 4);
+    const int M = p.ovl_sms;
+    auto bw = [&](float x) { return fminf(p.ovl_sm_bps * x, p.ovl_peak_bps * x / (x + p.ovl_half_sms)); };
+    // key: the time's bits (non-negative floats order as unsigned) above x
+    unsigned long long key = ~0ull;
+    for (int x = tid + 1; x < M; x += 1024) {
+      const float t = fmaxf(bytes / bw((float)x), flops / ((float)(M - x) * p.ovl_flops_sm));
+      const unsigned long long k = ((unsigned long long)__float_as_uint(t) << 32) | (unsigned)x;
+      key = k < key ? k : key;
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(FULL_MASK, key, off);
+      key = o < key ? o : key;
+    }
+    if (lane == 0) best[wid] = key;
+    __syncthreads();
     if (tid == 0) {
-      // in seconds x SMs (single precision: a few digits decide an SM count)
-      const float A = (float)dec_tok * (float)(p.num_kv_heads * p.head_dim * 4) / p.ovl_peak_bps;
-      const float F = (float)ch_pairs * (float)(p.num_q_heads * p.head_dim * 4) / p.ovl_flops_sm;
-      const float M = (float)p.ovl_sms, h = p.ovl_half_sms;
-      float x = M;
-      if (A <= 0.f) x = 0.f;
-      else if (F > 0.f) {
-        const float bq = A * M - A * h - F;
-        x = (bq + sqrtf(bq * bq + 4.f * A * A * h * M)) / (2.f * A);
-      }
+      for (int i = 1; i < 32; ++i) key = best[i] < key ? best[i] : key;
       const int gcta = p.grid / p.ovl_wg;   // decode CTAs launched
-      int xi = (int)ceilf(x);
-      xi = xi < 0 ? 0 : (xi > gcta ? gcta : xi);
-      if (A > 0.0 && xi == 0) xi = 1;
+      int xi = gcta;                        // the passes in turn
+      if (bytes <= 0.f) xi = 0;             // no decode rows: every SM to the chunks
+      else if (flops > 0.f && key != ~0ull) {
+        const float t_best = __uint_as_float((unsigned)(key >> 32));
+        const float t_turn = bytes / bw((float)M) + flops / ((float)M * p.ovl_flops_sm);
+        if (t_best < (1.f - p.ovl_margin) * t_turn) xi = (int)(key & 0xffffffffu);
+      }
+      xi = xi > gcta ? gcta : xi;
       active = (unsigned)(xi * p.ovl_wg);
     }
   }

@@ -92,9 +92,11 @@ struct DecodeParams {
   int overlap = 0;
   int ovl_wg = 1;                // decoders per CTA (set at launch)
   int ovl_sms = 0;               // SMs of the device (set at launch)
-  float ovl_peak_bps = 0.f;      // decode bandwidth model: peak * x / (x + half) on x SMs
+  float ovl_sm_bps = 0.f;        // decode bandwidth model on x SMs:
+  float ovl_peak_bps = 0.f;      //   min(sm_bps * x, peak * x / (x + half))
   float ovl_half_sms = 0.f;
   float ovl_flops_sm = 0.f;      // chunked pass: flop/s per SM
+  float ovl_margin = 0.f;        // side by side only when predicted this much faster
 };
 
 // Launch the work-list pass and the decode pass for one cache dtype /
