@@ -47,31 +47,57 @@ def _batch(Hq, Hkv, prior, counts, N, seed=700, D=128, B=16, dtype=torch.bfloat1
     return w, step, ref, dev
 
 
-def _call(pkv, out, w, dev, max_query_len, pt=256):
+def _call(pkv, out, w, dev, max_query_len, pt=256, workspace=None):
     pkv.paged_attention_mixed(out, dev["q"], dev["k"], dev["v"], dev["tab"], dev["lens"],
                               dev["qs"], w.scale, max_query_len=max_query_len,
-                              partition_tokens=pt)
+                              partition_tokens=pt, workspace=workspace)
 
 
-def test_stream_order_and_repeats_without_synchronising():
-    """64 long decode rows (split over partitions, merged at the end) and two
-    short chunks: the chunked pass ends long before the decode pass.  Each of
-    ten calls is followed at once, on the same stream, by a copy of out;
-    only after all of them does the host wait.  Every copy equals the first,
-    which matches the oracle."""
+def _workspace(pkv, w, step, dev, pt=256):
+    n = pkv.paged_attention_workspace_bytes(len(step.lens), w.num_q_heads, w.head_dim,
+                                            dev["tab"].shape[1] * w.block_size, pt)
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def _decode_sms(ws):
+    """SMs the last call's work list kept for the decode rows (word 2 of the
+    workspace's control block: decoders, three to an SM)."""
+    return int(ws[:16].view(torch.int32)[2].item()) // 3
+
+
+@pytest.mark.parametrize("chunks", ["two short", "eight of 256"])
+def test_stream_order_and_repeats_without_synchronising(chunks):
+    """64 long decode rows (split over partitions, merged at the end) and
+    prompt chunks.  With two short chunks the decode pass keeps every SM
+    (side by side would gain too little) and the chunked CTAs follow; with
+    eight chunks of 256 tokens the split is real (about 99 SMs for the
+    decode rows) and the two passes end close together, in either order.
+    Each of ten calls is followed at once, on the same stream, by a copy of
+    out; only after all of them does the host wait.  Every copy equals the
+    first, which matches the oracle."""
     import paged_kv_cache_117_gb300 as pkv
-    prior = [3000 + 37 * i for i in range(64)] + [100, 700]
-    counts = [1] * 64 + [96, 130]
+    if chunks == "two short":
+        prior = [3000 + 37 * i for i in range(64)] + [100, 700]
+        counts = [1] * 64 + [96, 130]
+    else:
+        prior = [3000 + 37 * i for i in range(64)] + [500 + 61 * j for j in range(8)]
+        counts = [1] * 64 + [256] * 8
     w, step, ref, dev = _batch(16, 2, prior, counts, N=18_000)
     T = step.query_start[-1]
     out = torch.empty((T, 16, 128), dtype=torch.float32, device="cuda")
+    ws = _workspace(pkv, w, step, dev)
     snaps = []
     for _ in range(10):
         out.fill_(float("nan"))
-        _call(pkv, out, w, dev, max(counts))
+        _call(pkv, out, w, dev, max(counts), workspace=ws)
         snaps.append(out.clone())
     torch.cuda.synchronize()
     assert pkv.read_device_flags(clear=True) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if chunks == "two short":
+        assert _decode_sms(ws) == sms
+    else:
+        assert 0 < _decode_sms(ws) < sms
     for snap in snaps[1:]:
         assert torch.equal(snap, snaps[0])
     gh.assert_close_to_oracle(snaps[0], ref, ATOL)
